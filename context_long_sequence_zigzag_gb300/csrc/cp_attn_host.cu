@@ -1,0 +1,552 @@
+// cp_attn_host.cu — host runtime of libcpattn: descriptor validation, the
+// shard map, the per-call tile plans (ring visiting order, causal skipping),
+// workspace layout and dispatch to the kernels.  Every exported function of
+// include/cp_attn.h is defined here.
+//
+// The shard map and block classes follow
+//   "Ulysses与Ring-Attention详解" §4.2 (zigzag: rank r holds chunk r and chunk
+//   2C-1-r) and "超长上下文训练速度翻倍秘籍" §2 pitfall 1 / §3 varlen CP (own
+//   diagonal block causal, earlier blocks unmasked, every packed sub-sequence
+//   cut into CP pieces), and "LLM context parallel production guide",
+//   "因果 Attention 会制造 Rank 负载不均" (blocks above the diagonal skipped).
+#include <algorithm>
+#include <cmath>
+#include <cstring>
+#include <mutex>
+#include <vector>
+
+#include "internal.h"
+
+namespace cpattn {
+namespace {
+
+struct Chunk {
+  int32_t seq, idx, pos0, len, rank;
+  int64_t grow0;  // first global row
+  int64_t srow0;  // first sharded row
+};
+
+struct ShardMap {
+  int32_t C = 0, S = 0, per = 0;  // ranks, sequences, chunks per rank per sequence
+  std::vector<Chunk> chunks;      // index (r * S + s) * per + k
+  std::vector<int64_t> rank_off;  // C + 1
+
+  const Chunk& at(int r, int s, int k) const { return chunks[(size_t(r) * S + s) * per + k]; }
+};
+
+std::vector<int32_t> seqlens_of(const cp_desc_t* d) {
+  std::vector<int32_t> cu;
+  if (d->cu_seqlens == nullptr) {
+    cu = {0, int32_t(d->total_tokens)};
+  } else {
+    cu.assign(d->cu_seqlens, d->cu_seqlens + d->num_seqs + 1);
+  }
+  return cu;
+}
+
+// Checks shared by every call that reads the shard map.
+cp_status_t check_map_fields(const cp_desc_t* d) {
+  if (d == nullptr) return CP_ERR_INVALID_ARG;
+  if (d->total_tokens < 0 || d->total_tokens > INT32_MAX) return CP_ERR_INVALID_ARG;
+  if (d->num_seqs < 1) return CP_ERR_INVALID_ARG;
+  if (d->cp_size < 1 || d->cp_size > 4096) return CP_ERR_INVALID_ARG;
+  if (d->layout != CP_LAYOUT_CONTIGUOUS && d->layout != CP_LAYOUT_ZIGZAG) return CP_ERR_INVALID_ARG;
+  if (d->cu_seqlens == nullptr) {
+    if (d->num_seqs != 1) return CP_ERR_INVALID_ARG;
+    return CP_OK;
+  }
+  const int32_t* cu = d->cu_seqlens;
+  if (cu[0] != 0) return CP_ERR_INVALID_ARG;
+  for (int s = 0; s < d->num_seqs; ++s)
+    if (cu[s + 1] < cu[s]) return CP_ERR_INVALID_ARG;
+  if (int64_t(cu[d->num_seqs]) != d->total_tokens) return CP_ERR_INVALID_ARG;
+  return CP_OK;
+}
+
+cp_status_t check_attn_fields(const cp_desc_t* d) {
+  cp_status_t st = check_map_fields(d);
+  if (st != CP_OK) return st;
+  if (d->hq < 1 || d->hkv < 1 || d->hq % d->hkv != 0) return CP_ERR_INVALID_ARG;
+  if (d->d_qk < 1 || d->d_v < 1) return CP_ERR_INVALID_ARG;
+  if (d->dtype != CP_DT_F32 && d->dtype != CP_DT_BF16) return CP_ERR_INVALID_ARG;
+  if (d->gqa != CP_GQA_BLOCKED && d->gqa != CP_GQA_INTERLEAVED) return CP_ERR_INVALID_ARG;
+  if (d->causal != 0 && d->causal != 1) return CP_ERR_INVALID_ARG;
+  if (!(d->scale > 0.f) || !std::isfinite(d->scale)) return CP_ERR_INVALID_ARG;
+  const int elt = d->dtype == CP_DT_BF16 ? 2 : 4;
+  if ((d->d_qk * elt) % 16 != 0 || (d->d_v * elt) % 16 != 0) return CP_ERR_INVALID_ARG;
+  // The CUDA-core path keeps head rows in registers spread over a warp.
+  if (d->d_qk > 256 || d->d_v > 256) return CP_ERR_UNSUPPORTED;
+  if (int64_t(d->total_tokens) * d->hq * std::max(d->d_qk, d->d_v) > (int64_t(1) << 40))
+    return CP_ERR_UNSUPPORTED;
+  return CP_OK;
+}
+
+ShardMap build_map(const cp_desc_t* d) {
+  ShardMap m;
+  std::vector<int32_t> cu = seqlens_of(d);
+  m.C = d->cp_size;
+  m.S = int32_t(cu.size()) - 1;
+  m.per = d->layout == CP_LAYOUT_ZIGZAG ? 2 : 1;
+  const int64_t n = int64_t(m.C) * m.per;  // pieces per sequence
+  m.chunks.reserve(size_t(m.C) * m.S * m.per);
+  m.rank_off.assign(m.C + 1, 0);
+  int64_t srow = 0;
+  for (int r = 0; r < m.C; ++r) {
+    m.rank_off[r] = srow;
+    for (int s = 0; s < m.S; ++s) {
+      const int64_t L = int64_t(cu[s + 1]) - cu[s];
+      for (int k = 0; k < m.per; ++k) {
+        const int64_t c = (k == 0) ? r : (2 * int64_t(m.C) - 1 - r);
+        const int64_t lo = (c * L) / n, hi = ((c + 1) * L) / n;
+        Chunk ch;
+        ch.seq = s;
+        ch.idx = int32_t(c);
+        ch.pos0 = int32_t(lo);
+        ch.len = int32_t(hi - lo);
+        ch.rank = r;
+        ch.grow0 = cu[s] + lo;
+        ch.srow0 = srow;
+        m.chunks.push_back(ch);
+        srow += hi - lo;
+      }
+    }
+  }
+  m.rank_off[m.C] = srow;
+  return m;
+}
+
+struct Plan {
+  std::vector<TileDesc> tiles;
+  std::vector<RangeDesc> ranges;
+  int32_t max_ranges = 0;
+};
+
+int32_t ceil_tiles(int64_t n) { return int32_t((n + kTile - 1) / kTile); }
+
+// Query-major plan: every query tile with the key runs it must visit, in ring
+// order r, r-1, ..., r-C+1 (mod C).  q_rank / kv_rank >= 0 restrict the plan
+// to one (query shard, key shard) block.
+Plan build_fwd_plan(const cp_desc_t* d, const ShardMap& m, int q_rank, int kv_rank) {
+  Plan p;
+  const bool causal = d->causal != 0;
+  for (const Chunk& A : m.chunks) {
+    if (q_rank >= 0 && A.rank != q_rank) continue;
+    for (int32_t t0 = 0; t0 < A.len; t0 += kTile) {
+      TileDesc t{};
+      t.row0 = int32_t(A.srow0 + t0);
+      t.nrows = std::min(kTile, A.len - t0);
+      t.pos0 = A.pos0 + t0;
+      t.rank = A.rank;
+      t.out_row0 = q_rank >= 0 ? int32_t(t.row0 - m.rank_off[q_rank]) : t.row0;
+      t.range_begin = int32_t(p.ranges.size());
+      const int32_t qmin = t.pos0, qmax = t.pos0 + t.nrows - 1;
+      int32_t work = 0;
+      for (int step = 0; step < m.C; ++step) {
+        const int rho = ((A.rank - step) % m.C + m.C) % m.C;
+        if (kv_rank >= 0 && rho != kv_rank) continue;
+        for (int k = 0; k < m.per; ++k) {
+          const Chunk& B = m.at(rho, A.seq, k);
+          if (B.len == 0) continue;
+          RangeDesc r{};
+          r.row0 = int32_t(B.srow0);
+          r.pos0 = B.pos0;
+          if (causal) {
+            if (B.pos0 > qmax) continue;  // entirely in the future: skipped
+            r.nrows = std::min(B.len, qmax - B.pos0 + 1);
+            r.flags = (B.pos0 + r.nrows - 1 > qmin) ? kRangeMasked : 0;
+          } else {
+            r.nrows = B.len;
+            r.flags = 0;
+          }
+          work += ceil_tiles(r.nrows);
+          p.ranges.push_back(r);
+        }
+      }
+      t.range_count = int32_t(p.ranges.size()) - t.range_begin;
+      t.work = work;
+      p.max_ranges = std::max(p.max_ranges, t.range_count);
+      p.tiles.push_back(t);
+    }
+  }
+  return p;
+}
+
+// Key-major plan for the backward: every key tile with the query runs that
+// see it, visiting ranks r, r+1, ... (the direction dK/dV travel in a ring).
+Plan build_bwd_plan(const cp_desc_t* d, const ShardMap& m) {
+  Plan p;
+  const bool causal = d->causal != 0;
+  for (const Chunk& B : m.chunks) {
+    for (int32_t t0 = 0; t0 < B.len; t0 += kTile) {
+      TileDesc t{};
+      t.row0 = int32_t(B.srow0 + t0);
+      t.nrows = std::min(kTile, B.len - t0);
+      t.pos0 = B.pos0 + t0;
+      t.rank = B.rank;
+      t.out_row0 = t.row0;
+      t.range_begin = int32_t(p.ranges.size());
+      const int32_t kmin = t.pos0, kmax = t.pos0 + t.nrows - 1;
+      int32_t work = 0;
+      for (int step = 0; step < m.C; ++step) {
+        const int rho = (B.rank + step) % m.C;
+        for (int k = 0; k < m.per; ++k) {
+          const Chunk& A = m.at(rho, B.seq, k);
+          if (A.len == 0) continue;
+          RangeDesc r{};
+          if (causal) {
+            if (A.pos0 + A.len - 1 < kmin) continue;  // every query precedes the keys
+            const int32_t skip = std::max(0, kmin - A.pos0);
+            r.row0 = int32_t(A.srow0 + skip);
+            r.nrows = A.len - skip;
+            r.pos0 = A.pos0 + skip;
+            r.flags = (r.pos0 < kmax) ? kRangeMasked : 0;
+          } else {
+            r.row0 = int32_t(A.srow0);
+            r.nrows = A.len;
+            r.pos0 = A.pos0;
+            r.flags = 0;
+          }
+          work += ceil_tiles(r.nrows);
+          p.ranges.push_back(r);
+        }
+      }
+      t.range_count = int32_t(p.ranges.size()) - t.range_begin;
+      t.work = work;
+      p.max_ranges = std::max(p.max_ranges, t.range_count);
+      p.tiles.push_back(t);
+    }
+  }
+  return p;
+}
+
+// Heaviest tiles first, so that the block scheduler starts the long ones
+// early (longest-processing-time order).
+void order_by_work(Plan& p) {
+  std::stable_sort(p.tiles.begin(), p.tiles.end(),
+                   [](const TileDesc& a, const TileDesc& b) { return a.work > b.work; });
+}
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+size_t plan_bytes(const Plan& p) {
+  return align256(p.tiles.size() * sizeof(TileDesc)) + align256(p.ranges.size() * sizeof(RangeDesc));
+}
+
+// Copies the plan into the workspace at `base`; returns the device pointers.
+cudaError_t upload_plan(const Plan& p, char* base, cudaStream_t st, const TileDesc** tiles,
+                        const RangeDesc** ranges) {
+  const size_t tb = p.tiles.size() * sizeof(TileDesc);
+  const size_t rb = p.ranges.size() * sizeof(RangeDesc);
+  char* rbase = base + align256(tb);
+  // Pageable source: the runtime stages the bytes before returning, so the
+  // vectors may be freed as soon as these calls return.
+  if (tb) {
+    cudaError_t e = cudaMemcpyAsync(base, p.tiles.data(), tb, cudaMemcpyHostToDevice, st);
+    if (e != cudaSuccess) return e;
+  }
+  if (rb) {
+    cudaError_t e = cudaMemcpyAsync(rbase, p.ranges.data(), rb, cudaMemcpyHostToDevice, st);
+    if (e != cudaSuccess) return e;
+  }
+  *tiles = reinterpret_cast<const TileDesc*>(base);
+  *ranges = reinterpret_cast<const RangeDesc*>(rbase);
+  return cudaSuccess;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+bool use_tc_fwd(const cp_desc_t* d) {
+  return d->dtype == CP_DT_BF16 && tc_fwd_supported(d->d_qk, d->d_v);
+}
+bool use_tc_bwd(const cp_desc_t* d) {
+  return d->dtype == CP_DT_BF16 && tc_bwd_supported(d->d_qk, d->d_v);
+}
+
+AttnArgs base_args(const cp_desc_t* d) {
+  AttnArgs a{};
+  a.T = d->total_tokens;
+  a.lse_stride = d->total_tokens;
+  a.hq = d->hq;
+  a.hkv = d->hkv;
+  a.d_qk = d->d_qk;
+  a.d_v = d->d_v;
+  a.gqa_interleaved = d->gqa == CP_GQA_INTERLEAVED;
+  a.causal = d->causal;
+  a.scale = d->scale;
+  return a;
+}
+
+struct BwdLayout {
+  size_t fwd_plan, bwd_plan, dpsum, dq_acc, total;
+};
+
+BwdLayout bwd_layout(const cp_desc_t* d, const Plan& pf, const Plan& pb) {
+  BwdLayout L{};
+  L.fwd_plan = 0;
+  L.bwd_plan = plan_bytes(pf);
+  L.dpsum = L.bwd_plan + plan_bytes(pb);
+  L.dq_acc = L.dpsum + align256(size_t(d->hq) * size_t(d->total_tokens) * 4);
+  L.total = L.dq_acc;
+  if (use_tc_bwd(d)) L.total += align256(size_t(d->total_tokens) * d->hq * d->d_qk * 4);
+  return L;
+}
+
+}  // namespace
+}  // namespace cpattn
+
+using namespace cpattn;
+
+extern "C" {
+
+const char* cp_status_string(cp_status_t s) {
+  switch (s) {
+    case CP_OK: return "CP_OK";
+    case CP_ERR_INVALID_ARG: return "CP_ERR_INVALID_ARG: invalid descriptor field, pointer or size";
+    case CP_ERR_UNSUPPORTED: return "CP_ERR_UNSUPPORTED: valid but not implemented";
+    case CP_ERR_CUDA: return "CP_ERR_CUDA: a CUDA runtime call or kernel launch failed";
+    case CP_ERR_DEVICE_TIMEOUT: return "CP_ERR_DEVICE_TIMEOUT: a bounded device wait ran out";
+    case CP_ERR_WORKSPACE: return "CP_ERR_WORKSPACE: workspace missing, misaligned or too small";
+  }
+  return "unknown cp_status_t";
+}
+
+cp_status_t cp_validate(const cp_desc_t* d) { return check_attn_fields(d); }
+
+cp_status_t cp_workspace_size(const cp_desc_t* d, int32_t op, size_t* bytes) {
+  if (bytes == nullptr) return CP_ERR_INVALID_ARG;
+  if (op == CP_OP_PERMUTE) {
+    cp_status_t st = check_map_fields(d);
+    if (st != CP_OK) return st;
+    const size_t nseg = size_t(d->cp_size) * d->num_seqs * (d->layout == CP_LAYOUT_ZIGZAG ? 2 : 1);
+    *bytes = align256(nseg * sizeof(CopySeg));
+    return CP_OK;
+  }
+  cp_status_t st = check_attn_fields(d);
+  if (st != CP_OK) return st;
+  ShardMap m = build_map(d);
+  if (op == CP_OP_FWD) {
+    *bytes = plan_bytes(build_fwd_plan(d, m, -1, -1));
+  } else if (op == CP_OP_BLOCK_FWD) {
+    // the largest (q rank, kv rank) plan is bounded by the plan of rank q's
+    // tiles against all ranks; size for the worst rank
+    size_t mx = 0;
+    for (int r = 0; r < m.C; ++r) mx = std::max(mx, plan_bytes(build_fwd_plan(d, m, r, -1)));
+    *bytes = mx;
+  } else if (op == CP_OP_BWD) {
+    *bytes = bwd_layout(d, build_fwd_plan(d, m, -1, -1), build_bwd_plan(d, m)).total;
+  } else {
+    return CP_ERR_INVALID_ARG;
+  }
+  return CP_OK;
+}
+
+cp_status_t cp_shard_offsets(const cp_desc_t* d, int64_t* offsets) {
+  cp_status_t st = check_map_fields(d);
+  if (st != CP_OK) return st;
+  if (offsets == nullptr) return CP_ERR_INVALID_ARG;
+  ShardMap m = build_map(d);
+  for (int r = 0; r <= m.C; ++r) offsets[r] = m.rank_off[r];
+  return CP_OK;
+}
+
+cp_status_t cp_rank_block_counts(const cp_desc_t* d, int64_t* counts) {
+  cp_status_t st = check_attn_fields(d);
+  if (st != CP_OK) return st;
+  if (counts == nullptr) return CP_ERR_INVALID_ARG;
+  ShardMap m = build_map(d);
+  Plan p = build_fwd_plan(d, m, -1, -1);
+  for (int r = 0; r < m.C; ++r) counts[r] = 0;
+  for (const TileDesc& t : p.tiles) counts[t.rank] += t.work;
+  return CP_OK;
+}
+
+cp_status_t cp_shard_permute(const cp_desc_t* d, const void* in, void* out, int64_t row_bytes,
+                             int32_t inverse, void* ws, size_t ws_bytes, cp_stream_t stream) {
+  cp_status_t st = check_map_fields(d);
+  if (st != CP_OK) return st;
+  if (row_bytes <= 0 || row_bytes % 16 != 0) return CP_ERR_INVALID_ARG;
+  if (inverse != 0 && inverse != 1) return CP_ERR_INVALID_ARG;
+  if (d->total_tokens == 0) return CP_OK;
+  if (in == nullptr || out == nullptr || !aligned16(in) || !aligned16(out)) return CP_ERR_INVALID_ARG;
+  const char* ib = static_cast<const char*>(in);
+  const char* ob = static_cast<const char*>(out);
+  const int64_t total = d->total_tokens * row_bytes;
+  if (ib < ob + total && ob < ib + total) return CP_ERR_INVALID_ARG;  // overlap
+  size_t need = 0;
+  cp_workspace_size(d, CP_OP_PERMUTE, &need);
+  if (ws == nullptr || (reinterpret_cast<uintptr_t>(ws) & 255) || ws_bytes < need) return CP_ERR_WORKSPACE;
+
+  ShardMap m = build_map(d);
+  std::vector<CopySeg> segs;
+  segs.reserve(m.chunks.size());
+  int64_t pieces = 0;
+  for (const Chunk& c : m.chunks) {
+    if (c.len == 0) continue;
+    CopySeg s;
+    const int64_t g = c.grow0 * row_bytes, sh = c.srow0 * row_bytes;
+    s.src = inverse ? sh : g;
+    s.dst = inverse ? g : sh;
+    s.bytes = int64_t(c.len) * row_bytes;
+    s.piece0 = pieces;
+    pieces += (s.bytes + kPermutePiece - 1) / kPermutePiece;
+    segs.push_back(s);
+  }
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  if (cudaMemcpyAsync(ws, segs.data(), segs.size() * sizeof(CopySeg), cudaMemcpyHostToDevice, cs) !=
+      cudaSuccess)
+    return CP_ERR_CUDA;
+  if (launch_permute(static_cast<const CopySeg*>(ws), int32_t(segs.size()), pieces, in, out, cs) !=
+      cudaSuccess)
+    return CP_ERR_CUDA;
+  return CP_OK;
+}
+
+cp_status_t cp_lse_merge(const cp_desc_t* d, int64_t rows, float* o_acc, float* lse_acc,
+                         const float* o_part, const float* lse_part, cp_stream_t stream) {
+  if (d == nullptr || rows < 0) return CP_ERR_INVALID_ARG;
+  if (d->hq < 1 || d->d_v < 4 || d->d_v % 4 != 0) return CP_ERR_INVALID_ARG;
+  if (rows == 0) return CP_OK;
+  if (!o_acc || !lse_acc || !o_part || !lse_part) return CP_ERR_INVALID_ARG;
+  if (!aligned16(o_acc) || !aligned16(o_part) || (reinterpret_cast<uintptr_t>(lse_acc) & 3) ||
+      (reinterpret_cast<uintptr_t>(lse_part) & 3))
+    return CP_ERR_INVALID_ARG;
+  if (launch_lse_merge(rows, d->hq, d->d_v, o_acc, lse_acc, o_part, lse_part,
+                       reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return CP_ERR_CUDA;
+  return CP_OK;
+}
+
+cp_status_t cp_attn_block_fwd(const cp_desc_t* d, int32_t q_rank, int32_t kv_rank, const void* q,
+                              const void* k, const void* v, float* o_part, float* lse_part, void* ws,
+                              size_t ws_bytes, cp_stream_t stream) {
+  cp_status_t st = check_attn_fields(d);
+  if (st != CP_OK) return st;
+  if (q_rank < 0 || q_rank >= d->cp_size || kv_rank < 0 || kv_rank >= d->cp_size)
+    return CP_ERR_INVALID_ARG;
+  ShardMap m = build_map(d);
+  const int64_t Tr = m.rank_off[q_rank + 1] - m.rank_off[q_rank];
+  if (Tr == 0) return CP_OK;
+  if (!q || !k || !v || !o_part || !lse_part) return CP_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o_part) || !aligned16(lse_part))
+    return CP_ERR_INVALID_ARG;
+  Plan p = build_fwd_plan(d, m, q_rank, kv_rank);
+  order_by_work(p);
+  if (ws == nullptr || (reinterpret_cast<uintptr_t>(ws) & 255) || ws_bytes < plan_bytes(p))
+    return CP_ERR_WORKSPACE;
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  AttnArgs a = base_args(d);
+  if (upload_plan(p, static_cast<char*>(ws), cs, &a.tiles, &a.ranges) != cudaSuccess) return CP_ERR_CUDA;
+  a.num_tiles = int32_t(p.tiles.size());
+  a.max_ranges = p.max_ranges;
+  a.q = q;
+  a.k = k;
+  a.v = v;
+  a.out = o_part;
+  a.lse = lse_part;
+  a.lse_stride = Tr;
+  a.block_mode = 1;
+  cudaError_t e = use_tc_fwd(d) ? launch_tc_fwd(a, cs) : launch_simt_fwd(a, d->dtype, cs);
+  return e == cudaSuccess ? CP_OK : CP_ERR_CUDA;
+}
+
+cp_status_t cp_attn_fwd(const cp_desc_t* d, const void* q, const void* k, const void* v, void* o,
+                        float* lse, void* ws, size_t ws_bytes, cp_stream_t stream) {
+  cp_status_t st = check_attn_fields(d);
+  if (st != CP_OK) return st;
+  if (d->total_tokens == 0) return CP_OK;
+  if (!q || !k || !v || !o || !lse) return CP_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
+    return CP_ERR_INVALID_ARG;
+  ShardMap m = build_map(d);
+  Plan p = build_fwd_plan(d, m, -1, -1);
+  order_by_work(p);
+  if (ws == nullptr || (reinterpret_cast<uintptr_t>(ws) & 255) || ws_bytes < plan_bytes(p))
+    return CP_ERR_WORKSPACE;
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  AttnArgs a = base_args(d);
+  if (upload_plan(p, static_cast<char*>(ws), cs, &a.tiles, &a.ranges) != cudaSuccess) return CP_ERR_CUDA;
+  a.num_tiles = int32_t(p.tiles.size());
+  a.max_ranges = p.max_ranges;
+  a.q = q;
+  a.k = k;
+  a.v = v;
+  a.out = o;
+  a.lse = lse;
+  cudaError_t e = use_tc_fwd(d) ? launch_tc_fwd(a, cs) : launch_simt_fwd(a, d->dtype, cs);
+  return e == cudaSuccess ? CP_OK : CP_ERR_CUDA;
+}
+
+cp_status_t cp_attn_bwd(const cp_desc_t* d, const void* q, const void* k, const void* v,
+                        const void* o, const float* lse, const void* dout, void* dq, void* dk,
+                        void* dv, void* ws, size_t ws_bytes, cp_stream_t stream) {
+  cp_status_t st = check_attn_fields(d);
+  if (st != CP_OK) return st;
+  if (d->total_tokens == 0) return CP_OK;
+  const void* ptrs[] = {q, k, v, o, lse, dout, dq, dk, dv};
+  for (const void* p : ptrs)
+    if (p == nullptr || !aligned16(p)) return CP_ERR_INVALID_ARG;
+  ShardMap m = build_map(d);
+  Plan pf = build_fwd_plan(d, m, -1, -1);
+  Plan pb = build_bwd_plan(d, m);
+  order_by_work(pf);
+  order_by_work(pb);
+  BwdLayout L = bwd_layout(d, pf, pb);
+  if (ws == nullptr || (reinterpret_cast<uintptr_t>(ws) & 255) || ws_bytes < L.total)
+    return CP_ERR_WORKSPACE;
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  char* base = static_cast<char*>(ws);
+  AttnArgs a = base_args(d);
+  a.q = q;
+  a.k = k;
+  a.v = v;
+  a.o = o;
+  a.lse_in = lse;
+  a.dout = dout;
+  a.dq = dq;
+  a.dk = dk;
+  a.dv = dv;
+  a.dpsum = reinterpret_cast<float*>(base + L.dpsum);
+  a.dq_acc = use_tc_bwd(d) ? reinterpret_cast<float*>(base + L.dq_acc) : nullptr;
+
+  if (launch_bwd_preprocess(a, d->dtype, cs) != cudaSuccess) return CP_ERR_CUDA;
+  if (use_tc_bwd(d)) {
+    if (upload_plan(pb, base + L.bwd_plan, cs, &a.tiles, &a.ranges) != cudaSuccess) return CP_ERR_CUDA;
+    a.num_tiles = int32_t(pb.tiles.size());
+    a.max_ranges = pb.max_ranges;
+    if (cudaMemsetAsync(a.dq_acc, 0, size_t(d->total_tokens) * d->hq * d->d_qk * 4, cs) != cudaSuccess)
+      return CP_ERR_CUDA;
+    if (launch_tc_bwd(a, cs) != cudaSuccess) return CP_ERR_CUDA;
+    if (launch_dq_postprocess(a, cs) != cudaSuccess) return CP_ERR_CUDA;
+    return CP_OK;
+  }
+  AttnArgs aq = a;
+  if (upload_plan(pf, base + L.fwd_plan, cs, &aq.tiles, &aq.ranges) != cudaSuccess) return CP_ERR_CUDA;
+  aq.num_tiles = int32_t(pf.tiles.size());
+  aq.max_ranges = pf.max_ranges;
+  if (launch_simt_bwd_dq(aq, d->dtype, cs) != cudaSuccess) return CP_ERR_CUDA;
+  AttnArgs ak = a;
+  if (upload_plan(pb, base + L.bwd_plan, cs, &ak.tiles, &ak.ranges) != cudaSuccess) return CP_ERR_CUDA;
+  ak.num_tiles = int32_t(pb.tiles.size());
+  ak.max_ranges = pb.max_ranges;
+  if (launch_simt_bwd_dkdv(ak, d->dtype, cs) != cudaSuccess) return CP_ERR_CUDA;
+  return CP_OK;
+}
+
+cp_status_t cp_device_status(cp_stream_t stream, int32_t* code) {
+  if (code == nullptr) return CP_ERR_INVALID_ARG;
+  if (read_and_clear_device_status(code, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return CP_ERR_CUDA;
+  return *code == 0 ? CP_OK : CP_ERR_DEVICE_TIMEOUT;
+}
+
+cp_status_t cp_check_bounded_wait(int64_t timeout_ns, int32_t* code, cp_stream_t stream) {
+  if (code == nullptr || timeout_ns < 100000 || timeout_ns > 5000000000LL) return CP_ERR_INVALID_ARG;
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  int32_t dummy = 0;
+  if (read_and_clear_device_status(&dummy, cs) != cudaSuccess) return CP_ERR_CUDA;
+  if (launch_wait_selftest(timeout_ns, cs) != cudaSuccess) return CP_ERR_CUDA;
+  if (read_and_clear_device_status(code, cs) != cudaSuccess) return CP_ERR_CUDA;
+  return CP_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,109 @@
+// internal.h — structures shared by the host runtime and the kernels of
+// libcpattn.  Not part of the public ABI (that is include/cp_attn.h).
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+#include <cuda_runtime.h>
+
+#include "cp_attn.h"
+
+namespace cpattn {
+
+// Rows per attention tile on both sides (queries and keys).
+constexpr int kTile = 128;
+
+// A tile: up to kTile consecutive SHARDED rows that hold consecutive
+// positions of one sequence (tiles never cross a chunk boundary).
+// In the forward plan a tile is a query tile and its ranges are key runs; in
+// the backward plan a tile is a key tile and its ranges are query runs.
+struct TileDesc {
+  int32_t row0;         // first sharded row
+  int32_t nrows;        // 1..kTile
+  int32_t pos0;         // position of row0 inside its sequence
+  int32_t range_begin;  // first entry in the range array
+  int32_t range_count;  // number of runs this tile visits, in ring order
+  int32_t out_row0;     // output row of row0 (block mode: relative to the shard)
+  int32_t work;         // number of kTile-row steps over all its runs
+  int32_t rank;         // virtual rank that owns the tile
+};
+static_assert(sizeof(TileDesc) == 32, "TileDesc layout");
+
+// A run: consecutive sharded rows holding consecutive positions of one
+// sequence, already clipped to the rows that can be visible to the tile.
+struct RangeDesc {
+  int32_t row0;   // first sharded row
+  int32_t nrows;  // > 0
+  int32_t pos0;   // position of row0 inside its sequence
+  int32_t flags;  // bit 0: some (tile row, run row) pair is causally masked
+};
+static_assert(sizeof(RangeDesc) == 16, "RangeDesc layout");
+
+constexpr int32_t kRangeMasked = 1;
+
+// One contiguous copy of the shard permutation (a chunk of one sequence).
+struct CopySeg {
+  int64_t src;     // byte offset in the source
+  int64_t dst;     // byte offset in the destination
+  int64_t bytes;   // length in bytes
+  int64_t piece0;  // index of the first 32 KiB piece of this segment
+};
+static_assert(sizeof(CopySeg) == 32, "CopySeg layout");
+
+constexpr int64_t kPermutePiece = 32768;
+
+// Kernel arguments of every attention launch.
+struct AttnArgs {
+  const void* q;
+  const void* k;
+  const void* v;
+  const void* o;     // forward output (read by the backward)
+  const void* dout;
+  void* out;         // forward: o (dtype) or o_part (f32, block mode)
+  float* lse;        // forward output / backward input, [hq, lse_stride]
+  const float* lse_in;
+  float* dpsum;      // backward: D = rowsum(dout * o), [hq, T]
+  float* dq_acc;     // backward: f32 [T, hq, d_qk]
+  void* dq;
+  void* dk;
+  void* dv;
+  const TileDesc* tiles;
+  const RangeDesc* ranges;
+  int32_t num_tiles;
+  int32_t max_ranges;  // longest range list of any tile
+  int64_t T;
+  int64_t lse_stride;  // T, or the shard's row count in block mode
+  int32_t hq, hkv, d_qk, d_v;
+  int32_t gqa_interleaved;
+  int32_t causal;
+  int32_t block_mode;
+  float scale;
+};
+
+// Device error word (bounded waits that ran out), defined in device_status.cu.
+enum : int32_t {
+  kErrNone = 0,
+  kErrWaitTimeoutBase = 0x100,  // | wait site id
+};
+
+// ---- launchers (each returns cudaSuccess or the launch error) ----
+cudaError_t launch_permute(const CopySeg* segs, int32_t nseg, int64_t npieces,
+                           const void* in, void* out, cudaStream_t st);
+cudaError_t launch_lse_merge(int64_t rows, int32_t hq, int32_t dv, float* o_acc, float* lse_acc,
+                             const float* o_part, const float* lse_part, cudaStream_t st);
+cudaError_t launch_simt_fwd(const AttnArgs& a, int32_t dtype, cudaStream_t st);
+cudaError_t launch_bwd_preprocess(const AttnArgs& a, int32_t dtype, cudaStream_t st);
+cudaError_t launch_simt_bwd_dq(const AttnArgs& a, int32_t dtype, cudaStream_t st);
+cudaError_t launch_simt_bwd_dkdv(const AttnArgs& a, int32_t dtype, cudaStream_t st);
+cudaError_t launch_dq_postprocess(const AttnArgs& a, cudaStream_t st);
+cudaError_t launch_tc_fwd(const AttnArgs& a, cudaStream_t st);
+cudaError_t launch_tc_bwd(const AttnArgs& a, cudaStream_t st);
+bool tc_fwd_supported(int32_t d_qk, int32_t d_v);
+bool tc_bwd_supported(int32_t d_qk, int32_t d_v);
+cudaError_t read_and_clear_device_status(int32_t* code, cudaStream_t st);
+// Device address of the error word on the current device (cached per device).
+int32_t* device_error_word();
+cudaError_t launch_wait_selftest(int64_t timeout_ns, cudaStream_t st);
+
+}  // namespace cpattn

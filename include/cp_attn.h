@@ -1,0 +1,208 @@
+/*
+ * cp_attn.h — C ABI of libcpattn: context-parallel exact causal attention on
+ * one GB300 (sm_103a).
+ *
+ * A sequence (or a pack of sequences) of T tokens is cut into C context-
+ * parallel shards.  The C "virtual ranks" all live on one GPU: the KV ring of
+ * ring attention is the order in which the kernels visit the KV shards that
+ * are already resident in device memory.  Sources for the method:
+ *   - "超长序列并行训练技术：Ulysses与Ring-Attention详解" (Ulysses and Ring-
+ *     Attention explained), §4.1 (blockwise attention: each (Q block, KV
+ *     block) step yields a partial output and its log-sum-exp, merged by an
+ *     update step), §4.2 (the lse merge formula; zigzag pairing of block i
+ *     with block 2C-1-i), §4.3 (the backward recomputes instead of storing).
+ *   - "超长上下文训练速度翻倍秘籍" (Ling long-context speed-up), §2 pitfall 1
+ *     (the local diagonal block is causal, KV blocks of earlier shards are
+ *     fully visible), §3 varlen CP (each packed sub-sequence is cut into CP
+ *     pieces, described by cu_seqlens).
+ *   - "LLM context parallel production guide" (oh-bug.com), sections
+ *     "核心原理" (exact merge through softmax statistics), "因果 Attention 会
+ *     制造 Rank 负载不均" (skip blocks above the diagonal; zigzag balances the
+ *     ranks; count effective QK blocks per rank), "变长序列" and
+ *     "位置编码必须跟序列分片一起走" (all position metadata follows the shard map).
+ *
+ * Conventions shared by every entry point
+ *   - Ownership: the caller owns every buffer; the library never allocates or
+ *     frees memory.  Device buffers are plain device pointers; the host
+ *     pointers are read during the call only.
+ *   - Streams: all GPU work is enqueued asynchronously on `stream` (a
+ *     cudaStream_t; NULL = the legacy default stream).  A call returns after
+ *     enqueueing; errors found on the host are returned before anything is
+ *     enqueued.  A status of CP_ERR_CUDA means a CUDA runtime call or a kernel
+ *     launch failed (cudaGetLastError is left as the runtime set it).
+ *   - Token order: every token-major tensor passed to the attention calls is in
+ *     SHARDED order: the concatenation of the C ranks' local buffers, rank 0
+ *     first.  cu_seqlens is always given in GLOBAL order; the library derives
+ *     the shard map from it.  cp_shard_permute converts between the orders.
+ *   - Shard map: sequence s of length L is cut into n pieces at floor(j*L/n),
+ *     j = 0..n (pieces differ by at most one token and may be empty).
+ *     CONTIGUOUS: n = C, rank r holds piece r.  ZIGZAG: n = 2C, rank r holds
+ *     piece r then piece 2C-1-r.  Inside a rank, sequences appear in order.
+ *   - Layouts (row-major, innermost last):
+ *       q [T, hq, d_qk]   k [T, hkv, d_qk]   v [T, hkv, d_v]
+ *       o, dout [T, hq, d_v]   dq [T, hq, d_qk]   dk [T, hkv, d_qk]   dv [T, hkv, d_v]
+ *       lse [hq, T] float32, natural log of the sum of exp(scale * q.k) over the
+ *       visible keys.  Element type of q/k/v/o/dout/dq/dk/dv = desc.dtype.
+ *   - Alignment: every tensor pointer must be 16-byte aligned and
+ *     d_qk * elt and d_v * elt must be multiples of 16 bytes.
+ *   - Visibility: key j is visible to query i iff they belong to the same
+ *     sequence and (causal == 0 or pos(j) <= pos(i)).  A query that sees no key
+ *     gets o = 0 and lse = -inf.
+ *   - GQA: hq % hkv == 0, G = hq / hkv.  BLOCKED: kv(h) = h / G.
+ *     INTERLEAVED: kv(h) = h % hkv.
+ *   - Precision: BF16 inputs run on the tcgen05 tensor cores with FP32
+ *     accumulation (d_qk in {128, 192}, d_v = 128); other head dims and FP32
+ *     inputs run on a CUDA-core FP32 path.  Outputs o/dq/dk/dv are rounded to
+ *     desc.dtype (round to nearest even); lse, partial outputs and the merge
+ *     are FP32.
+ */
+#ifndef CP_ATTN_H
+#define CP_ATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t, declared here so that this header needs no CUDA
+ * header. */
+typedef struct CUstream_st* cp_stream_t;
+
+typedef enum {
+  CP_OK = 0,
+  CP_ERR_INVALID_ARG = 1,    /* a descriptor field, pointer or size is invalid   */
+  CP_ERR_UNSUPPORTED = 2,    /* valid but not implemented (e.g. head dim)        */
+  CP_ERR_CUDA = 3,           /* a CUDA runtime call or kernel launch failed      */
+  CP_ERR_DEVICE_TIMEOUT = 4, /* a kernel's bounded wait ran out (see cp_device_status) */
+  CP_ERR_WORKSPACE = 5       /* workspace pointer NULL/misaligned or too small   */
+} cp_status_t;
+
+typedef enum { CP_LAYOUT_CONTIGUOUS = 0, CP_LAYOUT_ZIGZAG = 1 } cp_layout_t;
+typedef enum { CP_DT_F32 = 0, CP_DT_BF16 = 1 } cp_dtype_t;
+typedef enum { CP_GQA_BLOCKED = 0, CP_GQA_INTERLEAVED = 1 } cp_gqa_t;
+typedef enum { CP_OP_FWD = 0, CP_OP_BWD = 1, CP_OP_BLOCK_FWD = 2, CP_OP_PERMUTE = 3 } cp_op_t;
+
+/* Problem descriptor.  Read on the host during each call; not retained. */
+typedef struct {
+  int64_t total_tokens;       /* T >= 0                                            */
+  int32_t num_seqs;           /* >= 1 packed sequences                             */
+  int32_t hq, hkv;            /* query heads, key/value heads (hq % hkv == 0)      */
+  const int32_t* cu_seqlens;  /* HOST, num_seqs+1 entries, global order: cu[0] = 0,
+                                 non-decreasing, cu[num_seqs] = T.  NULL is allowed
+                                 only with num_seqs == 1 (one sequence of T).      */
+  int32_t d_qk, d_v;          /* head dims of q/k and v/o                          */
+  int32_t cp_size;            /* C >= 1 virtual ranks                              */
+  int32_t layout;             /* cp_layout_t                                       */
+  int32_t causal;             /* 1: causal inside each sequence, 0: full           */
+  float scale;                /* softmax scale applied to q.k (> 0, finite)        */
+  int32_t gqa;                /* cp_gqa_t                                          */
+  int32_t dtype;              /* cp_dtype_t of q/k/v/o/dout/dq/dk/dv               */
+} cp_desc_t;
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char* cp_status_string(cp_status_t status);
+
+/* Check a descriptor on the host (no GPU work).  Returns CP_OK,
+ * CP_ERR_INVALID_ARG or CP_ERR_UNSUPPORTED. */
+cp_status_t cp_validate(const cp_desc_t* desc);
+
+/* Workspace bytes needed by one call of operation `op` (cp_op_t) for this
+ * descriptor.  Host only.  The workspace must be device memory, 256-byte
+ * aligned, at least this large, and must not be used by anything else while
+ * the call's kernels run. */
+cp_status_t cp_workspace_size(const cp_desc_t* desc, int32_t op, size_t* bytes);
+
+/* Start row of every rank's shard in sharded order: offsets[0..C], host
+ * array of C+1 int64 (offsets[C] = T).  Host only. */
+cp_status_t cp_shard_offsets(const cp_desc_t* desc, int64_t* offsets);
+
+/* Effective attention work per virtual rank: the number of visible
+ * (128-query x 128-key) tiles that rank's queries touch for one head, host
+ * array of C int64.  "LLM context parallel production guide", 因果 Attention
+ * 会制造 Rank 负载不均: monitor effective QK blocks per rank, not tokens.
+ * Host only. */
+cp_status_t cp_rank_block_counts(const cp_desc_t* desc, int64_t* counts);
+
+/* Bit-exact row permutation between global and sharded order
+ * ("Ulysses与Ring-Attention详解" §4.2 zigzag table; "LLM context parallel
+ * production guide", 位置编码必须跟序列分片一起走: every token-major tensor —
+ * q, k, v, positions, masks, labels — follows the same map).
+ *   in, out    : device, T rows of row_bytes bytes each; must not overlap
+ *   row_bytes  : > 0, multiple of 16; in/out 16-byte aligned
+ *   inverse    : 0 = global -> sharded, 1 = sharded -> global
+ *   workspace  : cp_workspace_size(desc, CP_OP_PERMUTE) bytes
+ * Only total_tokens, num_seqs, cu_seqlens, cp_size and layout are read. */
+cp_status_t cp_shard_permute(const cp_desc_t* desc, const void* in, void* out,
+                             int64_t row_bytes, int32_t inverse,
+                             void* workspace, size_t workspace_bytes, cp_stream_t stream);
+
+/* One ring step: the queries of rank q_rank against the keys/values held by
+ * rank kv_rank ("Ulysses与Ring-Attention详解" §4.1 compute_block -> (out, lse);
+ * "超长上下文训练速度翻倍秘籍" §2: the q_rank == kv_rank block is causal, keys of
+ * earlier positions are fully visible, later ones are skipped).
+ *   q, k, v   : full sharded tensors; only the two ranks' rows are read
+ *   o_part    : device float32 [T_r, hq, d_v], T_r = rows of rank q_rank;
+ *               normalised over the visible keys of this block
+ *   lse_part  : device float32 [hq, T_r]; -inf (with o_part = 0) for rows that
+ *               see no key of this block
+ *   workspace : cp_workspace_size(desc, CP_OP_BLOCK_FWD) bytes */
+cp_status_t cp_attn_block_fwd(const cp_desc_t* desc, int32_t q_rank, int32_t kv_rank,
+                              const void* q, const void* k, const void* v,
+                              float* o_part, float* lse_part,
+                              void* workspace, size_t workspace_bytes, cp_stream_t stream);
+
+/* In-place exact merge of a partial result into an accumulator
+ * ("Ulysses与Ring-Attention详解" §4.2: lse = log(exp(lse_acc) + exp(lse_part));
+ * o = exp(lse_acc - lse) o_acc + exp(lse_part - lse) o_part).  -inf is the
+ * identity (an empty partial leaves the accumulator unchanged).
+ *   rows      : number of token rows (e.g. T_r of one rank)
+ *   o_acc, o_part     : device float32 [rows, hq, d_v]
+ *   lse_acc, lse_part : device float32 [hq, rows]
+ * Only hq and d_v (multiple of 4) are read from desc. */
+cp_status_t cp_lse_merge(const cp_desc_t* desc, int64_t rows,
+                         float* o_acc, float* lse_acc,
+                         const float* o_part, const float* lse_part, cp_stream_t stream);
+
+/* Fused forward over all ranks: for every rank's queries, the KV shards are
+ * visited in ring order r, r-1, ..., r-C+1 (mod C) with the merge done on
+ * chip; fully masked tiles are skipped.
+ *   q, k, v   : device, sharded order
+ *   o         : device [T, hq, d_v] (desc.dtype)
+ *   lse       : device float32 [hq, T] (kept for the backward)
+ *   workspace : cp_workspace_size(desc, CP_OP_FWD) bytes */
+cp_status_t cp_attn_fwd(const cp_desc_t* desc, const void* q, const void* k, const void* v,
+                        void* o, float* lse,
+                        void* workspace, size_t workspace_bytes, cp_stream_t stream);
+
+/* Backward ("Ulysses与Ring-Attention详解" §4.3): recomputes the attention
+ * probabilities from q, k and the stored final lse, with D = rowsum(dout * o),
+ * and writes dq, dk, dv (dk/dv summed over the query heads of each GQA group).
+ *   o, lse    : outputs of cp_attn_fwd for the same inputs
+ *   dout      : device [T, hq, d_v]
+ *   dq, dk, dv: device, sharded order, desc.dtype
+ *   workspace : cp_workspace_size(desc, CP_OP_BWD) bytes */
+cp_status_t cp_attn_bwd(const cp_desc_t* desc, const void* q, const void* k, const void* v,
+                        const void* o, const float* lse, const void* dout,
+                        void* dq, void* dk, void* dv,
+                        void* workspace, size_t workspace_bytes, cp_stream_t stream);
+
+/* Synchronises `stream`, then returns and clears the device error word of
+ * the current device: *code = 0 when every bounded wait since the last call
+ * completed, otherwise a nonzero code naming the wait that ran out (and the
+ * status CP_ERR_DEVICE_TIMEOUT). */
+cp_status_t cp_device_status(cp_stream_t stream, int32_t* code);
+
+/* Self-check of the bounded-wait machinery: launches one kernel that waits
+ * on a barrier nothing ever completes, with a limit of timeout_ns
+ * nanoseconds (1e5 .. 5e9), and reports through *code what the kernel saw
+ * (expected: the timeout code).  Synchronises `stream`.  Leaves the device
+ * error word cleared. */
+cp_status_t cp_check_bounded_wait(int64_t timeout_ns, int32_t* code, cp_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* CP_ATTN_H */

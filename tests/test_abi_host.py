@@ -1,0 +1,133 @@
+"""Host-side checks of the C ABI (no GPU needed): the library loads, exports
+every function include/cp_attn.h declares, validates descriptors, and its
+shard map and per-rank block counts agree with the oracle's shard order."""
+
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+import oracle
+import workloads
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+cpa = pytest.importorskip("context_long_sequence_zigzag_gb300")
+
+
+def _declared_functions():
+    src = open(os.path.join(ROOT, "include", "cp_attn.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(cp_[a-z_]+)\s*\(", src)))
+
+
+def test_library_exports_every_declared_function():
+    names = _declared_functions()
+    assert len(names) >= 12
+    lib = ctypes.CDLL(cpa.LIB_PATH)
+    for n in names:
+        assert hasattr(lib, n), n
+    assert sorted(cpa.EXPORTED) == names
+
+
+def test_status_strings():
+    for s in range(6):
+        assert cpa.cp_status_string(s).startswith("CP_")
+    assert "unknown" in cpa.cp_status_string(99)
+
+
+def _prob(**kw):
+    base = dict(total_tokens=1024, hq=8, hkv=2, d_qk=128, d_v=128, cp_size=4, layout="zigzag")
+    base.update(kw)
+    return cpa.Problem(**base)
+
+
+def test_validation():
+    assert cpa.cp_validate(_prob()) == cpa.CP_OK
+    assert cpa.cp_validate(_prob(hq=6, hkv=4)) == cpa.CP_ERR_INVALID_ARG
+    assert cpa.cp_validate(_prob(cp_size=0)) == cpa.CP_ERR_INVALID_ARG
+    assert cpa.cp_validate(_prob(d_qk=264, d_v=128)) == cpa.CP_ERR_UNSUPPORTED
+    p = _prob(total_tokens=10, cu_seqlens=[0, 6, 4, 10])  # non-monotone
+    assert cpa.cp_validate(p) == cpa.CP_ERR_INVALID_ARG
+    p = _prob(total_tokens=11, cu_seqlens=[0, 6, 10])  # does not end at T
+    assert cpa.cp_validate(p) == cpa.CP_ERR_INVALID_ARG
+    p = _prob(d_qk=4, d_v=4)  # 8-byte rows violate the 16-byte rule
+    assert cpa.cp_validate(p) == cpa.CP_ERR_INVALID_ARG
+    p = _prob()
+    p.desc.scale = float("nan")
+    assert cpa.cp_validate(p) == cpa.CP_ERR_INVALID_ARG
+    p = _prob()
+    p.desc.layout = 7
+    assert cpa.cp_validate(p) == cpa.CP_ERR_INVALID_ARG
+
+
+def test_null_descriptor_and_workspace_errors():
+    lib = ctypes.CDLL(cpa.LIB_PATH)
+    lib.cp_validate.argtypes = [ctypes.c_void_p]
+    assert lib.cp_validate(None) == cpa.CP_ERR_INVALID_ARG
+    with pytest.raises(cpa.CpError):
+        cpa.cp_workspace_size(_prob(hq=3, hkv=2), cpa.CP_OP_FWD)
+
+
+@pytest.mark.parametrize("layout", ["contiguous", "zigzag"])
+@pytest.mark.parametrize("lengths", [[1000], [1, 2, 7, 64, 65, 300, 5], [4096, 31, 4097]])
+@pytest.mark.parametrize("C", [1, 2, 3, 8])
+def test_shard_offsets_match_oracle(layout, lengths, C):
+    cu = workloads.make_cu_seqlens(lengths).tolist()
+    p = _prob(total_tokens=cu[-1], cu_seqlens=cu, cp_size=C, layout=layout)
+    assert cpa.cp_shard_offsets(p) == oracle.rank_offsets(cu, C, layout).tolist()
+
+
+def _tile_pairs_oracle(cu, C, layout):
+    """Visible 128x128 (query tile, key tile) pairs per rank, counted from the
+    oracle's shard order: tiles are cut per chunk from its first row."""
+    perm = oracle.shard_order(cu, C, layout)
+    off = oracle.rank_offsets(cu, C, layout)
+    n = C if layout == "contiguous" else 2 * C
+    counts = []
+    for r in range(C):
+        tot = 0
+        for s in range(len(cu) - 1):
+            L = cu[s + 1] - cu[s]
+            b = oracle.chunk_bounds(L, n)
+            mine = oracle.rank_chunks(r, C, layout)
+            for ca in mine:
+                for t0 in range(b[ca], b[ca + 1], 128):
+                    qmax = min(t0 + 128, b[ca + 1]) - 1
+                    for cb in range(n):
+                        lo, hi = b[cb], b[cb + 1]
+                        if hi <= lo or lo > qmax:
+                            continue
+                        vis = min(hi - lo, qmax - lo + 1)
+                        tot += -(-vis // 128)
+        counts.append(tot)
+    del perm, off
+    return counts
+
+
+@pytest.mark.parametrize("layout", ["contiguous", "zigzag"])
+def test_rank_block_counts(layout):
+    cu = [0, 8192]
+    p = _prob(total_tokens=8192, cu_seqlens=cu, cp_size=4, layout=layout)
+    got = cpa.cp_rank_block_counts(p)
+    assert got == _tile_pairs_oracle(cu, 4, layout)
+    if layout == "zigzag":
+        assert len(set(got)) == 1  # zigzag balances the causal work
+    else:
+        assert got == sorted(got) and got[0] < got[-1]
+    lengths = workloads.varlen_lengths(20000, 64, 4000, 3)
+    cu = workloads.make_cu_seqlens(lengths).tolist()
+    p = _prob(total_tokens=cu[-1], cu_seqlens=cu, cp_size=4, layout=layout)
+    assert cpa.cp_rank_block_counts(p) == _tile_pairs_oracle(cu, 4, layout)
+
+
+def test_workspace_sizes_positive_and_ordered():
+    p = _prob()
+    f = cpa.cp_workspace_size(p, cpa.CP_OP_FWD)
+    b = cpa.cp_workspace_size(p, cpa.CP_OP_BWD)
+    assert f > 0 and b > f
+    assert cpa.cp_workspace_size(p, cpa.CP_OP_PERMUTE) >= 32
+    with pytest.raises(cpa.CpError):
+        cpa.cp_workspace_size(p, 9)
