@@ -30,7 +30,7 @@ LIB_PATH = os.path.join(_HERE, "libcpattn.so")
 if not os.path.exists(LIB_PATH):
     raise ImportError(
         f"{LIB_PATH} is missing: build it with "
-        "`python -m context_long_sequence_zigzag_gb300.build` (no CPU fallback exists)")
+        "`python context_long_sequence_zigzag_gb300/build.py` (no CPU fallback exists)")
 
 _lib = ctypes.CDLL(LIB_PATH)
 

@@ -1,6 +1,6 @@
 """Builds libcpattn.so in-tree (next to this file) with nvcc for sm_103a.
 
-    python -m context_long_sequence_zigzag_gb300.build
+    python context_long_sequence_zigzag_gb300/build.py
 
 Each translation unit is compiled in parallel into ``_build/`` and linked
 into one shared library with the CUDA runtime linked statically, so the
@@ -12,6 +12,7 @@ from __future__ import annotations
 
 import concurrent.futures as cf
 import os
+import platform
 import shutil
 import subprocess
 import sys
@@ -20,7 +21,7 @@ PKG = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
-BUILD = os.path.join(PKG, "_build")
+BUILD = os.path.join(PKG, "_build", platform.machine())
 LIB = os.path.join(PKG, "libcpattn.so")
 
 SOURCES = [
