@@ -1,0 +1,371 @@
+"""Throughput benchmark: context-parallel causal attention, forward + backward.
+
+Workload (default): bf16, one 65536-token sequence, 32 query / 8 key-value
+heads (GQA), head dim 128, cut into 8 context-parallel shards in the zigzag
+layout; q, k, v, dout iid N(0, 1) (synthetic, seeded).
+
+One step = the whole hot path on one batch: shard permutation of q, k, v,
+dout (global -> sharded order), the fused forward (o, lse), the backward
+(dq, dk, dv), and the permutation of o, dq, dk, dv back to global order.
+``value`` counts attention FLOPs only over visible (query, key) pairs:
+fwd = pairs * hq * (2 d_qk + 2 d_v), bwd = pairs * hq * (6 d_qk + 4 d_v).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+N > 1 runs under torchrun, one process per GPU, each GPU an independent
+replica of the workload (the path needs no exchange on one node: the KV ring
+is a visiting order over shards already in device memory).
+``--impl reference`` times the float64 CPU oracle on a bounded sample of the
+same workload instead.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+import workloads  # noqa: E402
+
+METRIC = "CP causal attn TFLOP/s fwd & fwd+bwd (bf16, S=64K) and % of GB300 BF16 peak"
+DEFAULT_WORKLOAD = "bf16_gqa_s64k_h32kv8_d128_c8_zigzag"
+FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            return json.load(f), "measured"
+    return dict(FALLBACK), "fallback"
+
+
+# ----------------------------------------------------------------------------- oracle (CPU baseline)
+
+def oracle_sample(w: workloads.Workload, budget_tokens: int = 8192):
+    """Times the float64 oracle's forward + backward on a bounded sample of the
+    workload: the first `budget_tokens` tokens of the stream and the query
+    heads of the first key/value head.  Returns (tflops, seconds, desc)."""
+    import oracle
+
+    lengths = w.lengths()
+    Ts = min(budget_tokens, w.total_tokens)
+    # the sample keeps the workload's sequence boundaries inside its prefix
+    cu = [0]
+    for L in lengths:
+        if cu[-1] >= Ts:
+            break
+        cu.append(min(Ts, cu[-1] + L))
+    G = w.hq // w.hkv
+    sub = w.replace(total_tokens=Ts, hq=G, hkv=1, seqlens=tuple(np.diff(cu).tolist()), varlen_range=None)
+    inp = workloads.make_inputs(sub, with_dout=True)
+    t0 = time.perf_counter()
+    oracle.attn_backward(inp["q"], inp["k"], inp["v"], inp["dout"], cu, w.scale, w.causal)
+    dt = time.perf_counter() - t0
+    flops = sub.flops_fwd() + sub.flops_bwd()
+    desc = (f"float64 oracle fwd+bwd on the first {Ts} tokens, {G} query heads / 1 kv head "
+            f"of the workload ({len(cu) - 1} sequence(s))")
+    return flops / dt / 1e12, dt, desc
+
+
+def cpu_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+# ----------------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------- GPU arm
+
+class Runner:
+    """Holds device buffers and runs one step of the hot path through the C ABI."""
+
+    def __init__(self, w: workloads.Workload, device: torch.device):
+        import context_long_sequence_zigzag_gb300 as cpa
+
+        self.cpa = cpa
+        self.w = w
+        self.dev = device
+        inp = workloads.make_inputs(w, device=device, with_dout=True)
+        self.cu = inp["cu_seqlens"].tolist()
+        self.prob = cpa.Problem(w.total_tokens, w.hq, w.hkv, w.d_qk, w.d_v, w.cp_size, w.layout, self.cu,
+                                w.causal, w.scale, "blocked", torch.bfloat16)
+        self.g = {n: inp[n] for n in ("q", "k", "v", "dout")}  # global order (inputs)
+        self.s = {n: torch.empty_like(t) for n, t in self.g.items()}  # sharded copies
+        T = w.total_tokens
+        bf = torch.bfloat16
+        self.o = torch.empty(T, w.hq, w.d_v, dtype=bf, device=device)
+        self.lse = torch.empty(w.hq, T, dtype=torch.float32, device=device)
+        self.dq = torch.empty(T, w.hq, w.d_qk, dtype=bf, device=device)
+        self.dk = torch.empty(T, w.hkv, w.d_qk, dtype=bf, device=device)
+        self.dv = torch.empty(T, w.hkv, w.d_v, dtype=bf, device=device)
+        self.out = {n: torch.empty_like(t) for n, t in
+                    (("o", self.o), ("dq", self.dq), ("dk", self.dk), ("dv", self.dv))}
+        self.ws_perm = cpa.workspace(self.prob, cpa.CP_OP_PERMUTE, device)
+        self.ws_fwd = cpa.workspace(self.prob, cpa.CP_OP_FWD, device)
+        self.ws_bwd = cpa.workspace(self.prob, cpa.CP_OP_BWD, device)
+        self.ev = []  # (fwd_start, fwd_end, bwd_start, bwd_end) per timed step
+        self.launches_per_step = 4 + 1 + 3 + 4  # permute x4, fwd, bwd (pre, main, post), permute x4
+
+    def step(self, record: bool = False):
+        cpa = self.cpa
+        for n in ("q", "k", "v", "dout"):
+            cpa.cp_shard_permute(self.prob, self.g[n], out=self.s[n], ws=self.ws_perm)
+        if record:
+            e = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+            e[0].record()
+        cpa.cp_attn_fwd(self.prob, self.s["q"], self.s["k"], self.s["v"], self.o, self.lse, self.ws_fwd)
+        if record:
+            e[1].record()
+            e[2].record()
+        cpa.cp_attn_bwd(self.prob, self.s["q"], self.s["k"], self.s["v"], self.o, self.lse, self.s["dout"],
+                        self.dq, self.dk, self.dv, self.ws_bwd)
+        if record:
+            e[3].record()
+            self.ev.append(e)
+        for n, t in (("o", self.o), ("dq", self.dq), ("dk", self.dk), ("dv", self.dv)):
+            cpa.cp_shard_permute(self.prob, t, inverse=True, out=self.out[n], ws=self.ws_perm)
+
+    def kernel_times_ms(self):
+        fwd = [a.elapsed_time(b) for a, b, _, _ in self.ev]
+        bwd = [c.elapsed_time(d) for _, _, c, d in self.ev]
+        return statistics.mean(fwd), statistics.mean(bwd)
+
+
+def e2e_measure(r: Runner, steps: int, warmup: int):
+    """Same metric through the ABI with host buffers: pinned host inputs are
+    copied in, the step runs, and o, dq, dk, dv are copied back each step."""
+    host_in = {n: t.cpu().pin_memory() for n, t in r.g.items()}
+    host_out = {n: torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for n, t in r.out.items()}
+    h2d = sum(t.numel() * t.element_size() for t in host_in.values())
+    d2h = sum(t.numel() * t.element_size() for t in host_out.values())
+
+    def one():
+        for n, t in host_in.items():
+            r.g[n].copy_(t, non_blocking=True)
+        r.step()
+        for n, t in host_out.items():
+            t.copy_(r.out[n], non_blocking=True)
+
+    for _ in range(warmup):
+        one()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(steps):
+        one()
+    e1.record()
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / steps, h2d, d2h
+
+
+def run_gpu(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    w = workloads.get(args.workload)
+    r = Runner(w, dev)
+    cpa = r.cpa
+
+    for _ in range(args.warmup):
+        r.step()
+    torch.cuda.synchronize()
+    if cpa.cp_device_status() != 0:
+        raise RuntimeError("device wait timeout during warm-up")
+
+    clocks = ClockSampler(local)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record()
+    for _ in range(args.steps):
+        r.step(record=True)
+    t1.record()
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    clk = clocks.stop()
+    ms = t0.elapsed_time(t1) / args.steps
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+    status = cpa.cp_device_status()
+    if status != 0:
+        raise RuntimeError(f"device wait timeout code {status:#x}")
+    fwd_ms, bwd_ms = r.kernel_times_ms()
+
+    e2e_ms, h2d, d2h = e2e_measure(r, max(1, min(args.steps, 3)), 1)
+
+    peaks, peak_kind = load_peaks()
+    peak_sus = float(peaks.get("bf16_tflops_sustained", FALLBACK["bf16_tflops_sustained"]))
+    peak_burst = float(peaks.get("bf16_tflops", FALLBACK["bf16_tflops"]))
+    f_fwd, f_bwd = w.flops_fwd(), w.flops_bwd()
+    value = (f_fwd + f_bwd) * world / (ms * 1e-3) / 1e12
+    fwd_tf = f_fwd / (fwd_ms * 1e-3) / 1e12
+    bwd_tf = f_bwd / (bwd_ms * 1e-3) / 1e12
+
+    result = None
+    if rank == 0:
+        traffic = None
+        prof = os.path.join(ROOT, "profiles", "attn_bwd_tc_traffic.json")
+        if os.path.exists(prof):
+            with open(prof) as f:
+                traffic = json.load(f).get("bytes_per_launch")
+        result = {
+            "metric": METRIC,
+            "value": round(value, 2),
+            "unit": "TFLOP/s",
+            "n_gpus": world,
+            "steps": args.steps,
+            "warmup": args.warmup,
+            "ms_per_step": round(ms, 3),
+            "higher_is_better": True,
+            "scaling": "weak",
+            "vs_baseline": None,
+            "dtype": "bf16",
+            "data": "synthetic (seeded iid N(0,1) q, k, v, dout)",
+            "config": {"workload": w.name, "total_tokens": w.total_tokens, "hq": w.hq, "hkv": w.hkv,
+                       "d_qk": w.d_qk, "d_v": w.d_v, "cp_size": w.cp_size, "layout": w.layout, "causal": w.causal,
+                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU, C virtual ranks",
+                       "l2": "inputs larger than L2 (q alone is 512 MiB)"},
+            "fwd_tflops": round(fwd_tf, 2),
+            "bwd_tflops": round(bwd_tf, 2),
+            "fwd_bwd_pct_of_peak": round(100 * value / world / peak_sus, 2),
+            "roofline": {"bound": "tensor", "kernel": "attn_bwd_tc (cp_attn_bwd)", "achieved": round(bwd_tf, 2),
+                         "peak": peak_sus, "unit": "TFLOP/s", "frac": round(bwd_tf / peak_sus, 4),
+                         "peak_kind": f"bf16 sustained, {peak_kind}", "traffic": traffic,
+                         "fwd": {"kernel": "attn_fwd_tc (cp_attn_fwd)", "achieved": round(fwd_tf, 2),
+                                 "frac": round(fwd_tf / peak_sus, 4),
+                                 "frac_of_burst": round(fwd_tf / peak_burst, 4)}},
+            "e2e": {"value": round((f_fwd + f_bwd) * world / (e2e_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 3)},
+            "clocks": clk,
+            "gpu_launches": r.launches_per_step * args.steps,
+            "rank_block_counts": cpa.cp_rank_block_counts(r.prob),
+        }
+        if not args.no_cpu_baseline:
+            tf, secs, desc = oracle_sample(w, args.cpu_tokens)
+            result["cpu_baseline"] = {"value": round(tf, 6), "unit": "TFLOP/s", "cores": cpu_cores(),
+                                      "kind": "oracle", "sample": desc, "seconds": round(secs, 2)}
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return result
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return None
+    w = workloads.get(args.workload)
+    vals = []
+    for _ in range(args.warmup):
+        oracle_sample(w, args.cpu_tokens // 2)
+    secs = []
+    desc = ""
+    for _ in range(args.steps):
+        tf, s, desc = oracle_sample(w, args.cpu_tokens // 2)
+        vals.append(tf)
+        secs.append(s)
+    v = statistics.mean(vals)
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(v, 6), "unit": "TFLOP/s", "n_gpus": 0,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1000 * statistics.mean(secs), 1),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded iid N(0,1) q, k, v, dout)",
+        "config": {"workload": w.name, "total_tokens": w.total_tokens, "hq": w.hq, "hkv": w.hkv, "d_qk": w.d_qk,
+                   "d_v": w.d_v, "cp_size": w.cp_size, "layout": w.layout},
+        "cpu_baseline": {"value": round(v, 6), "unit": "TFLOP/s", "cores": cpu_cores(), "kind": "oracle",
+                         "sample": desc},
+        "e2e": {"value": round(v, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=list(workloads.WORKLOADS))
+    ap.add_argument("--cpu-tokens", type=int, default=8192)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        res = run_reference(args)
+    else:
+        res = run_gpu(args)
+    if res is not None:
+        print(json.dumps(res), flush=True)
+
+
+if __name__ == "__main__":
+    main()
