@@ -44,6 +44,7 @@ EXPORTED = [
     "cp_status_string", "cp_validate", "cp_workspace_size", "cp_shard_offsets",
     "cp_rank_block_counts", "cp_shard_permute", "cp_attn_block_fwd", "cp_lse_merge",
     "cp_attn_fwd", "cp_attn_bwd", "cp_device_status", "cp_check_bounded_wait",
+    "cp_attn_fwd_noalloc",
 ]
 
 
@@ -81,6 +82,7 @@ _sigs = {
     "cp_attn_bwd": (ctypes.c_int, [_DP, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
     "cp_device_status": (ctypes.c_int, [_P, ctypes.POINTER(ctypes.c_int32)]),
     "cp_check_bounded_wait": (ctypes.c_int, [ctypes.c_int64, ctypes.POINTER(ctypes.c_int32), _P]),
+    "cp_attn_fwd_noalloc": (ctypes.c_int, [_DP, _P, _P, _P, _P, _P, _P]),
 }
 for _name, (_res, _args) in _sigs.items():
     _f = getattr(_lib, _name)
@@ -256,6 +258,18 @@ def cp_attn_bwd(prob: Problem, q, k, v, o, lse, dout, dq=None, dk=None, dv=None,
     _check(_lib.cp_attn_bwd(prob.ptr, _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout), _ptr(dq),
                             _ptr(dk), _ptr(dv), _ptr(ws), ws.numel(), _stream(stream)), "cp_attn_bwd")
     return dq, dk, dv
+
+
+def cp_attn_fwd_noalloc(prob: Problem, q, k, v, o, lse, stream=None):
+    """Forward without a workspace: the tile plan lives in the library's fixed
+    device scratch (CP_NOALLOC_SCRATCH_BYTES).  o and lse are caller-owned;
+    nothing is allocated here or in the library."""
+    _check(_lib.cp_attn_fwd_noalloc(prob.ptr, _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _stream(stream)),
+           "cp_attn_fwd_noalloc")
+    return o, lse
+
+
+NOALLOC_SCRATCH_BYTES = 4 << 20
 
 
 def cp_device_status(stream=None) -> int:

@@ -294,6 +294,38 @@ BwdLayout bwd_layout(const cp_desc_t* d, const Plan& pf, const Plan& pb) {
 }  // namespace
 }  // namespace cpattn
 
+// Fixed scratch of cp_attn_fwd_noalloc: the only device memory that entry
+// point needs beyond the caller's tensors is the tile plan, kept here.  The
+// symbol is a host-side stand-in in host code; its device address is looked
+// up once per device below.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[CP_NOALLOC_SCRATCH_BYTES];
+
+namespace cpattn {
+namespace {
+
+// Device address of g_noalloc_scratch on the current device, looked up on
+// the first call for that device (with the device current).
+cudaError_t noalloc_scratch(void** out) {
+  static std::mutex mu;
+  static void* ptrs[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(mu);
+  if (ptrs[dev] == nullptr) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess) return e;
+    ptrs[dev] = p;
+  }
+  *out = ptrs[dev];
+  return cudaSuccess;
+}
+
+}  // namespace
+}  // namespace cpattn
+
 using namespace cpattn;
 
 extern "C" {
@@ -530,6 +562,34 @@ cp_status_t cp_attn_bwd(const cp_desc_t* d, const void* q, const void* k, const 
   ak.max_ranges = pb.max_ranges;
   if (launch_simt_bwd_dkdv(ak, d->dtype, cs) != cudaSuccess) return CP_ERR_CUDA;
   return CP_OK;
+}
+
+cp_status_t cp_attn_fwd_noalloc(const cp_desc_t* d, const void* q, const void* k, const void* v, void* o,
+                                float* lse, cp_stream_t stream) {
+  cp_status_t st = check_attn_fields(d);
+  if (st != CP_OK) return st;
+  if (d->total_tokens == 0) return CP_OK;
+  ShardMap m = build_map(d);
+  Plan p = build_fwd_plan(d, m, -1, -1);
+  order_by_work(p);
+  if (plan_bytes(p) > CP_NOALLOC_SCRATCH_BYTES) return CP_ERR_WORKSPACE;
+  if (!q || !k || !v || !o || !lse) return CP_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
+    return CP_ERR_INVALID_ARG;
+  void* scratch = nullptr;
+  if (noalloc_scratch(&scratch) != cudaSuccess) return CP_ERR_CUDA;
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  AttnArgs a = base_args(d);
+  if (upload_plan(p, static_cast<char*>(scratch), cs, &a.tiles, &a.ranges) != cudaSuccess) return CP_ERR_CUDA;
+  a.num_tiles = int32_t(p.tiles.size());
+  a.max_ranges = p.max_ranges;
+  a.q = q;
+  a.k = k;
+  a.v = v;
+  a.out = o;
+  a.lse = lse;
+  cudaError_t e = use_tc_fwd(d) ? launch_tc_fwd(a, cs) : launch_simt_fwd(a, d->dtype, cs);
+  return e == cudaSuccess ? CP_OK : CP_ERR_CUDA;
 }
 
 cp_status_t cp_device_status(cp_stream_t stream, int32_t* code) {

@@ -188,6 +188,29 @@ cp_status_t cp_attn_bwd(const cp_desc_t* desc, const void* q, const void* k, con
                         void* dq, void* dk, void* dv,
                         void* workspace, size_t workspace_bytes, cp_stream_t stream);
 
+/* Forward without a workspace, for callers that cannot allocate device
+ * memory.  The source pages have no counterpart to this entry point.
+ *
+ * Some callers cannot call cudaMalloc (or any allocator): a plugin whose host
+ * framework owns every device allocation and hands it only its input and
+ * output tensors, or code on a path where allocating is not allowed.  This
+ * variant computes exactly what cp_attn_fwd computes, with the same arguments
+ * minus the workspace: its only scratch, the tile plan, lives in a
+ * fixed-size array inside the library's device image (CP_NOALLOC_SCRATCH_BYTES
+ * = 4 MiB, held by every GPU that loads the library until the process
+ * exits).  It calls no cudaMalloc, cudaFree or allocating routine.
+ *   - The first call on a device looks up the array's device address (once
+ *     per device, on the current device); make that first call before any
+ *     stream capture.
+ *   - A problem whose plan needs more than CP_NOALLOC_SCRATCH_BYTES is
+ *     rejected with CP_ERR_WORKSPACE before any GPU work is enqueued.
+ *   - Every call shares the one array and overwrites it with its own plan:
+ *     calls whose GPU work overlaps in time (different streams without
+ *     ordering) race on it.  Order such calls on one stream or with events. */
+#define CP_NOALLOC_SCRATCH_BYTES (4u << 20)
+cp_status_t cp_attn_fwd_noalloc(const cp_desc_t* desc, const void* q, const void* k, const void* v,
+                                void* o, float* lse, cp_stream_t stream);
+
 /* Synchronises `stream`, then returns and clears the device error word of
  * the current device: *code = 0 when every bounded wait since the last call
  * completed, otherwise a nonzero code naming the wait that ran out (and the
