@@ -162,7 +162,7 @@ class Runner:
         self.ws_fwd = cpa.workspace(self.prob, cpa.CP_OP_FWD, device)
         self.ws_bwd = cpa.workspace(self.prob, cpa.CP_OP_BWD, device)
         self.ev = []  # (fwd_start, fwd_end, bwd_start, bwd_end) per timed step
-        self.launches_per_step = 4 + 1 + 3 + 4  # permute x4, fwd, bwd (pre, main, post), permute x4
+        self.launches_per_step = 4 + 1 + 3 + 4  # permute x4, fwd, bwd (D pre-pass, dK/dV, dQ), permute x4
 
     def step(self, record: bool = False):
         cpa = self.cpa
@@ -300,7 +300,7 @@ def run_gpu(args):
             "fwd_tflops": round(fwd_tf, 2),
             "bwd_tflops": round(bwd_tf, 2),
             "fwd_bwd_pct_of_peak": round(100 * value / world / peak_sus, 2),
-            "roofline": {"bound": "tensor", "kernel": "attn_bwd_tc (cp_attn_bwd)", "achieved": round(bwd_tf, 2),
+            "roofline": {"bound": "tensor", "kernel": "attn_bwd (cp_attn_bwd: D pre-pass, dK/dV and dQ tcgen05 kernels)", "achieved": round(bwd_tf, 2),
                          "peak": peak_sus, "unit": "TFLOP/s", "frac": round(bwd_tf / peak_sus, 4),
                          "peak_kind": f"bf16 sustained, {peak_kind}", "traffic": traffic,
                          "fwd": {"kernel": "attn_fwd_tc (cp_attn_fwd)", "achieved": round(fwd_tf, 2),

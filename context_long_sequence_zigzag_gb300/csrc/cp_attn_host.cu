@@ -277,7 +277,7 @@ AttnArgs base_args(const cp_desc_t* d) {
 }
 
 struct BwdLayout {
-  size_t fwd_plan, bwd_plan, dpsum, dq_acc, total;
+  size_t fwd_plan, bwd_plan, dpsum, total;
 };
 
 BwdLayout bwd_layout(const cp_desc_t* d, const Plan& pf, const Plan& pb) {
@@ -285,9 +285,7 @@ BwdLayout bwd_layout(const cp_desc_t* d, const Plan& pf, const Plan& pb) {
   L.fwd_plan = 0;
   L.bwd_plan = plan_bytes(pf);
   L.dpsum = L.bwd_plan + plan_bytes(pb);
-  L.dq_acc = L.dpsum + align256(size_t(d->hq) * size_t(d->total_tokens) * 4);
-  L.total = L.dq_acc;
-  if (use_tc_bwd(d)) L.total += align256(size_t(d->total_tokens) * d->hq * d->d_qk * 4);
+  L.total = L.dpsum + align256(size_t(d->hq) * size_t(d->total_tokens) * 4);
   return L;
 }
 
@@ -538,17 +536,20 @@ cp_status_t cp_attn_bwd(const cp_desc_t* d, const void* q, const void* k, const 
   a.dk = dk;
   a.dv = dv;
   a.dpsum = reinterpret_cast<float*>(base + L.dpsum);
-  a.dq_acc = use_tc_bwd(d) ? reinterpret_cast<float*>(base + L.dq_acc) : nullptr;
 
   if (launch_bwd_preprocess(a, d->dtype, cs) != cudaSuccess) return CP_ERR_CUDA;
   if (use_tc_bwd(d)) {
-    if (upload_plan(pb, base + L.bwd_plan, cs, &a.tiles, &a.ranges) != cudaSuccess) return CP_ERR_CUDA;
-    a.num_tiles = int32_t(pb.tiles.size());
-    a.max_ranges = pb.max_ranges;
-    if (cudaMemsetAsync(a.dq_acc, 0, size_t(d->total_tokens) * d->hq * d->d_qk * 4, cs) != cudaSuccess)
-      return CP_ERR_CUDA;
-    if (launch_tc_bwd(a, cs) != cudaSuccess) return CP_ERR_CUDA;
-    if (launch_dq_postprocess(a, cs) != cudaSuccess) return CP_ERR_CUDA;
+    // dK, dV over the key-major plan; dQ over the query-major plan
+    AttnArgs ak = a;
+    if (upload_plan(pb, base + L.bwd_plan, cs, &ak.tiles, &ak.ranges) != cudaSuccess) return CP_ERR_CUDA;
+    ak.num_tiles = int32_t(pb.tiles.size());
+    ak.max_ranges = pb.max_ranges;
+    if (launch_tc_bwd_dkdv(ak, cs) != cudaSuccess) return CP_ERR_CUDA;
+    AttnArgs aq = a;
+    if (upload_plan(pf, base + L.fwd_plan, cs, &aq.tiles, &aq.ranges) != cudaSuccess) return CP_ERR_CUDA;
+    aq.num_tiles = int32_t(pf.tiles.size());
+    aq.max_ranges = pf.max_ranges;
+    if (launch_tc_bwd_dq(aq, cs) != cudaSuccess) return CP_ERR_CUDA;
     return CP_OK;
   }
   AttnArgs aq = a;

@@ -64,7 +64,6 @@ struct AttnArgs {
   float* lse;        // forward output / backward input, [hq, lse_stride]
   const float* lse_in;
   float* dpsum;      // backward: D = rowsum(dout * o), [hq, T]
-  float* dq_acc;     // backward: f32 [T, hq, d_qk]
   void* dq;
   void* dk;
   void* dv;
@@ -96,9 +95,10 @@ cudaError_t launch_simt_fwd(const AttnArgs& a, int32_t dtype, cudaStream_t st);
 cudaError_t launch_bwd_preprocess(const AttnArgs& a, int32_t dtype, cudaStream_t st);
 cudaError_t launch_simt_bwd_dq(const AttnArgs& a, int32_t dtype, cudaStream_t st);
 cudaError_t launch_simt_bwd_dkdv(const AttnArgs& a, int32_t dtype, cudaStream_t st);
-cudaError_t launch_dq_postprocess(const AttnArgs& a, cudaStream_t st);
 cudaError_t launch_tc_fwd(const AttnArgs& a, cudaStream_t st);
-cudaError_t launch_tc_bwd(const AttnArgs& a, cudaStream_t st);
+// tensor-core backward: dK/dV over the key-major plan, dQ over the query-major plan
+cudaError_t launch_tc_bwd_dkdv(const AttnArgs& a, cudaStream_t st);
+cudaError_t launch_tc_bwd_dq(const AttnArgs& a, cudaStream_t st);
 bool tc_fwd_supported(int32_t d_qk, int32_t d_v);
 bool tc_bwd_supported(int32_t d_qk, int32_t d_v);
 cudaError_t read_and_clear_device_status(int32_t* code, cudaStream_t st);

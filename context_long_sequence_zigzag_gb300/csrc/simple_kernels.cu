@@ -335,23 +335,6 @@ __global__ void __launch_bounds__(256) simt_bwd_dkdv_kernel(const AttnArgs a) {
   }
 }
 
-// dq (FP32 accumulator, already scaled) -> BF16, 8 elements per thread.
-__global__ void __launch_bounds__(256) dq_postprocess_kernel(const float* __restrict__ acc,
-                                                             __nv_bfloat16* __restrict__ dq,
-                                                             int64_t n8) {
-  for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < n8;
-       i += int64_t(gridDim.x) * blockDim.x) {
-    const float4 x = __ldcs(reinterpret_cast<const float4*>(acc) + 2 * i);
-    const float4 y = __ldcs(reinterpret_cast<const float4*>(acc) + 2 * i + 1);
-    __nv_bfloat162 r[4];
-    r[0] = __floats2bfloat162_rn(x.x, x.y);
-    r[1] = __floats2bfloat162_rn(x.z, x.w);
-    r[2] = __floats2bfloat162_rn(y.x, y.y);
-    r[3] = __floats2bfloat162_rn(y.z, y.w);
-    __stcs(reinterpret_cast<int4*>(dq) + i, *reinterpret_cast<int4*>(r));
-  }
-}
-
 int64_t grid_for(int64_t work_items, int per_block) {
   int64_t g = (work_items + per_block - 1) / per_block;
   const int64_t cap = int64_t(sm_count()) * 16;
@@ -416,14 +399,6 @@ cudaError_t launch_simt_bwd_dkdv(const AttnArgs& a, int32_t dtype, cudaStream_t 
     simt_bwd_dkdv_kernel<float><<<unsigned(grid), 256, 0, st>>>(a);
   else
     simt_bwd_dkdv_kernel<__nv_bfloat16><<<unsigned(grid), 256, 0, st>>>(a);
-  return cudaGetLastError();
-}
-
-cudaError_t launch_dq_postprocess(const AttnArgs& a, cudaStream_t st) {
-  const int64_t n = a.T * a.hq * a.d_qk;  // d_qk * 2 bytes is a multiple of 16
-  const int64_t n8 = n / 8;
-  const int64_t grid = grid_for(n8, 256);
-  dq_postprocess_kernel<<<unsigned(grid), 256, 0, st>>>(a.dq_acc, static_cast<__nv_bfloat16*>(a.dq), n8);
   return cudaGetLastError();
 }
 
