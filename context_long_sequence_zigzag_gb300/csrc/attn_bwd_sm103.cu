@@ -28,9 +28,12 @@
 //   of one head and visits the key tiles of the forward plan; dQ accumulates
 //   in TMEM over all of them and is written once.  Per step:
 //     [0,128)   S = Q K^T (SS)
-//     [128,256) dP = dO V^T (SS); then dS (bf16) in [128,160), [224,256)
+//     [128,256) dP = dO V^T (SS)
 //     [256,384) dQ += dS K (TS)
-//   MMA order S(j+1) as soon as S(j) has been read, then dQ(j), dP(j+1).
+//     [384,448), [448,512)  dS (bf16), double-buffered across steps
+//   S(j+1) is issued as soon as S(j) has been read and dP(j+1) as soon as
+//   dP(j) has been read, ahead of dQ(j), so the tensor pipe keeps working
+//   while the softmax warps turn S into P and dP into dS.
 //
 // In both kernels two groups of four compute warps split the N = 128 columns
 // (group g owns 64g..64g+63, thread = TMEM lane); each group writes its bf16
@@ -482,13 +485,15 @@ struct KvCursor {
 };
 
 struct DqCfg {
-  static constexpr int NS = 2;  // stages of (K, V)
+  // K(j) is read by S(j) and, one step later in issue order, by dQ(j); V(j)
+  // only by dP(j): K gets the deeper ring.
+  static constexpr int NSK = 3, NSV = 2;
   static constexpr uint32_t offQ = 0;
   static constexpr uint32_t offO = offQ + kTileBytes;
-  static constexpr uint32_t offK = offO + kTileBytes;       // NS stages
-  static constexpr uint32_t offV = offK + NS * kTileBytes;  // NS stages
-  static constexpr uint32_t offBar = offV + NS * kTileBytes;
-  static constexpr int kNumBars = 1 + 2 * NS + 6;
+  static constexpr uint32_t offK = offO + kTileBytes;        // NSK stages
+  static constexpr uint32_t offV = offK + NSK * kTileBytes;  // NSV stages
+  static constexpr uint32_t offBar = offV + NSV * kTileBytes;
+  static constexpr int kNumBars = 1 + 2 * NSK + 2 * NSV + 9;
   static constexpr uint32_t kSmem = offBar + kNumBars * 8 + 16;
   static_assert(kSmem <= 232448, "shared memory budget");
 };
@@ -511,22 +516,33 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dq_kernel(const __grid_c
 
   const uint32_t bar0 = sbase + Cfg::offBar;
   const uint32_t bar_q = bar0;
-  auto bar_kv_full = [&](int s) { return bar0 + 8u * (1 + s); };
-  auto bar_kv_empty = [&](int s) { return bar0 + 8u * (1 + Cfg::NS + s); };
-  const uint32_t bar_s_full = bar0 + 8u * (1 + 2 * Cfg::NS);
+  auto bar_k_full = [&](int s) { return bar0 + 8u * (1 + s); };
+  auto bar_k_empty = [&](int s) { return bar0 + 8u * (1 + Cfg::NSK + s); };
+  auto bar_v_full = [&](int s) { return bar0 + 8u * (1 + 2 * Cfg::NSK + s); };
+  auto bar_v_empty = [&](int s) { return bar0 + 8u * (1 + 2 * Cfg::NSK + Cfg::NSV + s); };
+  const uint32_t bar_s_full = bar0 + 8u * (1 + 2 * Cfg::NSK + 2 * Cfg::NSV);
   const uint32_t bar_dp_full = bar_s_full + 8;
   const uint32_t bar_p_full = bar_s_full + 16;
   const uint32_t bar_ds_full = bar_s_full + 24;
   const uint32_t bar_final = bar_s_full + 32;
   const uint32_t bar_drain = bar_s_full + 40;
+  const uint32_t bar_dp_read = bar_s_full + 48;                   // compute warps hold dP(j)
+  auto bar_dq_done = [&](int b) { return bar_s_full + 56 + 8u * b; };  // dQ(j) read dS buffer b = j & 1
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Cfg::offBar + Cfg::kNumBars * 8);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Cfg::offBar + Cfg::kNumBars * 8 + 4);
 
   if (threadIdx.x == 0) {
+    ptx::mbar_init(bar_dp_read, 8);
+    ptx::mbar_init(bar_dq_done(0), 1);
+    ptx::mbar_init(bar_dq_done(1), 1);
     ptx::mbar_init(bar_q, 1);
-    for (int s = 0; s < Cfg::NS; ++s) {
-      ptx::mbar_init(bar_kv_full(s), 1);
-      ptx::mbar_init(bar_kv_empty(s), 1);
+    for (int s = 0; s < Cfg::NSK; ++s) {
+      ptx::mbar_init(bar_k_full(s), 1);
+      ptx::mbar_init(bar_k_empty(s), 1);
+    }
+    for (int s = 0; s < Cfg::NSV; ++s) {
+      ptx::mbar_init(bar_v_full(s), 1);
+      ptx::mbar_init(bar_v_empty(s), 1);
     }
     ptx::mbar_init(bar_s_full, 1);
     ptx::mbar_init(bar_dp_full, 1);
@@ -562,26 +578,32 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dq_kernel(const __grid_c
         ptx::tma_load_3d(sbase + Cfg::offQ + c * kPanel, &p.tq, bar_q, c * 64, h, tile.row0);
         ptx::tma_load_3d(sbase + Cfg::offO + c * kPanel, &p.tdo, bar_q, c * 64, h, tile.row0);
       }
+      int issued_v = 0;
       KvCursor cur;
       cur.init(a.ranges, tile.range_begin, tile.range_count);
       for (int j = 0; j < n_kv; ++j, cur.next()) {
-        const int s = j % Cfg::NS;
-        if (j >= Cfg::NS && !ptx::mbar_wait(bar_kv_empty(s), ((j / Cfg::NS) - 1) & 1, kSiteKVEmpty, wctx)) break;
-        ptx::mbar_arrive_expect_tx(bar_kv_full(s), 2 * kTileBytes);
-        for (int c = 0; c < 2; ++c) {
-          ptx::tma_load_3d(sbase + Cfg::offK + s * kTileBytes + c * kPanel, &p.tk, bar_kv_full(s), c * 64, kvh,
+        const int sk = j % Cfg::NSK, sv = j % Cfg::NSV;
+        if (j >= Cfg::NSK && !ptx::mbar_wait(bar_k_empty(sk), ((j / Cfg::NSK) - 1) & 1, kSiteKVEmpty, wctx)) break;
+        ptx::mbar_arrive_expect_tx(bar_k_full(sk), kTileBytes);
+        for (int c = 0; c < 2; ++c)
+          ptx::tma_load_3d(sbase + Cfg::offK + sk * kTileBytes + c * kPanel, &p.tk, bar_k_full(sk), c * 64, kvh,
                            cur.row());
-          ptx::tma_load_3d(sbase + Cfg::offV + s * kTileBytes + c * kPanel, &p.tv, bar_kv_full(s), c * 64, kvh,
-                           cur.row());
-        }
         ++issued;
+        if (j >= Cfg::NSV && !ptx::mbar_wait(bar_v_empty(sv), ((j / Cfg::NSV) - 1) & 1, kSiteKVEmpty, wctx)) break;
+        ptx::mbar_arrive_expect_tx(bar_v_full(sv), kTileBytes);
+        for (int c = 0; c < 2; ++c)
+          ptx::tma_load_3d(sbase + Cfg::offV + sv * kTileBytes + c * kPanel, &p.tv, bar_v_full(sv), c * 64, kvh,
+                           cur.row());
+        ++issued_v;
       }
       if (*abort_flag) {
         volatile int no_abort = 0;
         const ptx::WaitCtx drain{&no_abort, nullptr, kWaitLimitNs};
         ptx::mbar_wait(bar_q, 0, kSiteDrain, drain);
-        for (int j = max(0, issued - Cfg::NS); j < issued; ++j)
-          ptx::mbar_wait(bar_kv_full(j % Cfg::NS), (j / Cfg::NS) & 1, kSiteDrain, drain);
+        for (int j = max(0, issued - Cfg::NSK); j < issued; ++j)
+          ptx::mbar_wait(bar_k_full(j % Cfg::NSK), (j / Cfg::NSK) & 1, kSiteDrain, drain);
+        for (int j = max(0, issued_v - Cfg::NSV); j < issued_v; ++j)
+          ptx::mbar_wait(bar_v_full(j % Cfg::NSV), (j / Cfg::NSV) & 1, kSiteDrain, drain);
       }
     }
   } else if (warp == 9) {
@@ -591,8 +613,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dq_kernel(const __grid_c
       constexpr uint32_t idQ = ptx::idesc_bf16_f32(BT, D, false, true);  // dQ: B = K as MN-major
       const uint32_t tS = tmem, tDP = tmem + 128, tDQ = tmem + 256;
       const uint32_t qb = sbase + Cfg::offQ, obb = sbase + Cfg::offO;
-      auto kb = [&](int j) { return sbase + Cfg::offK + (j % Cfg::NS) * kTileBytes; };
-      auto vb = [&](int j) { return sbase + Cfg::offV + (j % Cfg::NS) * kTileBytes; };
+      auto kb = [&](int j) { return sbase + Cfg::offK + (j % Cfg::NSK) * kTileBytes; };
+      auto vb = [&](int j) { return sbase + Cfg::offV + (j % Cfg::NSV) * kTileBytes; };
       auto issue_ss = [&](uint32_t d, uint32_t abase, uint32_t bbase) {
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
@@ -601,39 +623,51 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dq_kernel(const __grid_c
                       kk > 0);
         }
       };
-      bool ok = ptx::mbar_wait(bar_q, 0, kSiteQ, wctx) && ptx::mbar_wait(bar_kv_full(0), 0, kSiteKVFull, wctx);
+      bool ok = ptx::mbar_wait(bar_q, 0, kSiteQ, wctx) && ptx::mbar_wait(bar_k_full(0), 0, kSiteKVFull, wctx);
       if (ok) {
         ptx::tc_fence_after();
         issue_ss(tS, qb, kb(0));
         ptx::mma_commit(bar_s_full);
+        ok = ptx::mbar_wait(bar_v_full(0), 0, kSiteKVFull, wctx);
+      }
+      if (ok) {
+        ptx::tc_fence_after();
         issue_ss(tDP, obb, vb(0));
         ptx::mma_commit(bar_dp_full);
+        ptx::mma_commit(bar_v_empty(0));
       }
       for (int j = 0; ok && j < n_kv; ++j) {
-        // S(j+1) as soon as the compute warps have read S(j)
-        if (!ptx::mbar_wait(bar_p_full, j & 1, kSitePFull, wctx)) { ok = false; break; }
         if (j + 1 < n_kv) {
-          if (!ptx::mbar_wait(bar_kv_full((j + 1) % Cfg::NS), ((j + 1) / Cfg::NS) & 1, kSiteKVFull, wctx)) {
+          // S(j+1) as soon as the compute warps have read S(j)
+          if (!ptx::mbar_wait(bar_p_full, j & 1, kSitePFull, wctx) ||
+              !ptx::mbar_wait(bar_k_full((j + 1) % Cfg::NSK), ((j + 1) / Cfg::NSK) & 1, kSiteKVFull, wctx)) {
             ok = false;
             break;
           }
           ptx::tc_fence_after();
           issue_ss(tS, qb, kb(j + 1));
           ptx::mma_commit(bar_s_full);
+          // dP(j+1) as soon as they have read dP(j)
+          if (!ptx::mbar_wait(bar_dp_read, j & 1, kSiteDPFull, wctx) ||
+              !ptx::mbar_wait(bar_v_full((j + 1) % Cfg::NSV), ((j + 1) / Cfg::NSV) & 1, kSiteKVFull, wctx)) {
+            ok = false;
+            break;
+          }
+          ptx::tc_fence_after();
+          issue_ss(tDP, obb, vb(j + 1));
+          ptx::mma_commit(bar_dp_full);
+          ptx::mma_commit(bar_v_empty((j + 1) % Cfg::NSV));
         }
-        // dQ(j) += dS(j) K(j)
+        // dQ(j) += dS(j) K(j), dS(j) in buffer j & 1
         if (!ptx::mbar_wait(bar_ds_full, j & 1, kSiteDSFull, wctx)) { ok = false; break; }
         ptx::tc_fence_after();
         const uint32_t kbj = kb(j);
+        const uint32_t tA = tmem + 384 + 64 * (j & 1);
 #pragma unroll
         for (int kk = 0; kk < BT / 16; ++kk)
-          ptx::mma_ts(tDQ, tDP + (kk < 4 ? kk * 8 : 96 + (kk - 4) * 8),
-                      ptx::sdesc_sw128(kbj + kk * 2048, kPanel, 1024), idQ, (j > 0 || kk > 0));
-        ptx::mma_commit(bar_kv_empty(j % Cfg::NS));
-        if (j + 1 < n_kv) {
-          issue_ss(tDP, obb, vb(j + 1));
-          ptx::mma_commit(bar_dp_full);
-        }
+          ptx::mma_ts(tDQ, tA + kk * 8, ptx::sdesc_sw128(kbj + kk * 2048, kPanel, 1024), idQ, (j > 0 || kk > 0));
+        ptx::mma_commit(bar_dq_done(j & 1));
+        ptx::mma_commit(bar_k_empty(j % Cfg::NSK));
       }
       if (ok) ptx::mma_commit(bar_final);
       if (!ok) {
@@ -650,7 +684,6 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dq_kernel(const __grid_c
     const uint32_t lane_base = uint32_t((warp & 3) * 32) << 16;
     const uint32_t tS = tmem + lane_base, tDP = tmem + lane_base + 128;
     const uint32_t colS = grp * 64;
-    const uint32_t colPk = grp ? 96 : 0;
     const float sl2 = a.scale * kLog2e;
     const bool row_ok = r < tile.nrows;
     const int qpos = tile.pos0 + r;
@@ -686,9 +719,19 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dq_kernel(const __grid_c
       if (!__all_sync(0xffffffffu, ptx::mbar_wait(bar_dp_full, j & 1, kSiteDPFull, wctx))) { ok = false; break; }
       ptx::tc_fence_after();
       ld64(tDP + colS, x0, x1);
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(bar_dp_read);  // dP(j) has been read
 #pragma unroll
       for (int c = 0; c < 64; ++c) pf[c] *= fmaf(pick(x0, x1, c), a.scale, -dsc);
-      st_bf16_64(tDP + colPk, pf);
+      // dS buffer j & 1 was last read by dQ(j - 2)
+      if (j >= 2 &&
+          !__all_sync(0xffffffffu, ptx::mbar_wait(bar_dq_done(j & 1), ((j - 2) >> 1) & 1, kSiteDSFull, wctx))) {
+        ok = false;
+        break;
+      }
+      ptx::tc_fence_after();
+      st_bf16_64(tmem + lane_base + 384 + 64 * (j & 1) + 32 * grp, pf);
       ptx::tmem_st_wait();
       ptx::tc_fence_before();
       __syncwarp();
