@@ -79,6 +79,30 @@ def oracle_sample(w: workloads.Workload, budget_tokens: int = 8192):
     return flops / dt / 1e12, dt, desc
 
 
+def recorded_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch of `kernel` from the committed ncu summary
+    (profiles/dram_traffic.txt), or None when none was recorded for this
+    kernel and workload or the kernel's source changed since the capture."""
+    import hashlib
+
+    path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
+    if not os.path.exists(path):
+        return None
+    src = {"attn_fwd_tc_kernel": "attn_fwd_sm103.cu", "attn_bwd_dkdv_kernel": "attn_bwd_sm103.cu",
+           "attn_bwd_dq_kernel": "attn_bwd_sm103.cu"}.get(kernel)
+    if src is None:
+        return None
+    with open(os.path.join(ROOT, "context_long_sequence_zigzag_gb300", "csrc", src), "rb") as f:
+        digest = hashlib.sha256(f.read()).hexdigest()[:16]
+    with open(path) as f:
+        for line in f:
+            fields = dict(tok.split("=", 1) for tok in line.split() if "=" in tok)
+            if fields.get("kernel") == kernel and fields.get("workload") == workload and \
+                    fields.get("source_sha256_16") == digest:
+                return int(float(fields["bytes_per_launch"]))
+    return None
+
+
 def cpu_cores() -> int:
     try:
         return len(os.sched_getaffinity(0))
@@ -161,32 +185,50 @@ class Runner:
         self.ws_perm = cpa.workspace(self.prob, cpa.CP_OP_PERMUTE, device)
         self.ws_fwd = cpa.workspace(self.prob, cpa.CP_OP_FWD, device)
         self.ws_bwd = cpa.workspace(self.prob, cpa.CP_OP_BWD, device)
+        self.ws_dkdv = cpa.workspace(self.prob, cpa.CP_OP_BWD_DKDV, device)
+        self.ws_dq = cpa.workspace(self.prob, cpa.CP_OP_BWD_DQ, device)
+        self.dpsum = torch.empty(w.hq, T, dtype=torch.float32, device=device)
         self.ev = []  # (fwd_start, fwd_end, bwd_start, bwd_end) per timed step
-        self.launches_per_step = 4 + 1 + 3 + 4  # permute x4, fwd, bwd (D pre-pass, dK/dV, dQ), permute x4
+        self.launches_per_step = 4 + 1 + 3 + 4  # permute x4, fwd, D pre-pass, dK/dV, dQ, permute x4
 
-    def step(self, record: bool = False):
+    def step(self, record: bool = False, combined_bwd: bool = False):
         cpa = self.cpa
         for n in ("q", "k", "v", "dout"):
             cpa.cp_shard_permute(self.prob, self.g[n], out=self.s[n], ws=self.ws_perm)
+        e = [torch.cuda.Event(enable_timing=True) for _ in range(5)] if record else None
         if record:
-            e = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
             e[0].record()
         cpa.cp_attn_fwd(self.prob, self.s["q"], self.s["k"], self.s["v"], self.o, self.lse, self.ws_fwd)
         if record:
             e[1].record()
-            e[2].record()
-        cpa.cp_attn_bwd(self.prob, self.s["q"], self.s["k"], self.s["v"], self.o, self.lse, self.s["dout"],
-                        self.dq, self.dk, self.dv, self.ws_bwd)
+        if combined_bwd:
+            cpa.cp_attn_bwd(self.prob, self.s["q"], self.s["k"], self.s["v"], self.o, self.lse, self.s["dout"],
+                            self.dq, self.dk, self.dv, self.ws_bwd)
+        else:
+            # the same kernels as cp_attn_bwd, called one by one so that each
+            # is timed on its own
+            cpa.cp_attn_bwd_prep(self.prob, self.o, self.s["dout"], self.dpsum)
+            if record:
+                e[2].record()
+            cpa.cp_attn_bwd_dkdv(self.prob, self.s["q"], self.s["k"], self.s["v"], self.lse, self.dpsum,
+                                 self.s["dout"], self.dk, self.dv, self.ws_dkdv)
+            if record:
+                e[3].record()
+            cpa.cp_attn_bwd_dq(self.prob, self.s["q"], self.s["k"], self.s["v"], self.lse, self.dpsum,
+                               self.s["dout"], self.dq, self.ws_dq)
         if record:
-            e[3].record()
+            e[4].record()
             self.ev.append(e)
         for n, t in (("o", self.o), ("dq", self.dq), ("dk", self.dk), ("dv", self.dv)):
             cpa.cp_shard_permute(self.prob, t, inverse=True, out=self.out[n], ws=self.ws_perm)
 
     def kernel_times_ms(self):
-        fwd = [a.elapsed_time(b) for a, b, _, _ in self.ev]
-        bwd = [c.elapsed_time(d) for _, _, c, d in self.ev]
-        return statistics.mean(fwd), statistics.mean(bwd)
+        """Mean device time of (fwd, whole bwd, dK/dV kernel, dQ kernel)."""
+        fwd = [e[0].elapsed_time(e[1]) for e in self.ev]
+        bwd = [e[1].elapsed_time(e[4]) for e in self.ev]
+        dkdv = [e[2].elapsed_time(e[3]) for e in self.ev]
+        dq = [e[3].elapsed_time(e[4]) for e in self.ev]
+        return statistics.mean(fwd), statistics.mean(bwd), statistics.mean(dkdv), statistics.mean(dq)
 
 
 def e2e_measure(r: Runner, steps: int, warmup: int):
@@ -200,7 +242,7 @@ def e2e_measure(r: Runner, steps: int, warmup: int):
     def one():
         for n, t in host_in.items():
             r.g[n].copy_(t, non_blocking=True)
-        r.step()
+        r.step(combined_bwd=True)
         for n, t in host_out.items():
             t.copy_(r.out[n], non_blocking=True)
 
@@ -261,7 +303,7 @@ def run_gpu(args):
     status = cpa.cp_device_status()
     if status != 0:
         raise RuntimeError(f"device wait timeout code {status:#x}")
-    fwd_ms, bwd_ms = r.kernel_times_ms()
+    fwd_ms, bwd_ms, dkdv_ms, dq_ms = r.kernel_times_ms()
 
     e2e_ms, h2d, d2h = e2e_measure(r, max(1, min(args.steps, 3)), 1)
 
@@ -272,14 +314,20 @@ def run_gpu(args):
     value = (f_fwd + f_bwd) * world / (ms * 1e-3) / 1e12
     fwd_tf = f_fwd / (fwd_ms * 1e-3) / 1e12
     bwd_tf = f_bwd / (bwd_ms * 1e-3) / 1e12
+    # work each kernel actually performs (its own GEMMs over visible pairs)
+    pairs_h = float(w.visible_pairs()) * w.hq
+    kernels = {
+        "attn_fwd_tc_kernel": (fwd_ms, pairs_h * (2 * w.d_qk + 2 * w.d_v)),
+        "attn_bwd_dkdv_kernel": (dkdv_ms, pairs_h * (4 * w.d_qk + 4 * w.d_v)),
+        "attn_bwd_dq_kernel": (dq_ms, pairs_h * (4 * w.d_qk + 2 * w.d_v)),
+    }
+    dom = max(kernels, key=lambda k: kernels[k][0])
+    dom_ms, dom_flops = kernels[dom]
+    dom_tf = dom_flops / (dom_ms * 1e-3) / 1e12
 
     result = None
     if rank == 0:
-        traffic = None
-        prof = os.path.join(ROOT, "profiles", "attn_bwd_tc_traffic.json")
-        if os.path.exists(prof):
-            with open(prof) as f:
-                traffic = json.load(f).get("bytes_per_launch")
+        traffic = recorded_traffic(dom, w.name)
         result = {
             "metric": METRIC,
             "value": round(value, 2),
@@ -300,12 +348,16 @@ def run_gpu(args):
             "fwd_tflops": round(fwd_tf, 2),
             "bwd_tflops": round(bwd_tf, 2),
             "fwd_bwd_pct_of_peak": round(100 * value / world / peak_sus, 2),
-            "roofline": {"bound": "tensor", "kernel": "attn_bwd (cp_attn_bwd: D pre-pass, dK/dV and dQ tcgen05 kernels)", "achieved": round(bwd_tf, 2),
-                         "peak": peak_sus, "unit": "TFLOP/s", "frac": round(bwd_tf / peak_sus, 4),
+            "roofline": {"bound": "tensor", "kernel": dom, "achieved": round(dom_tf, 2), "peak": peak_sus,
+                         "unit": "TFLOP/s", "frac": round(dom_tf / peak_sus, 4),
                          "peak_kind": f"bf16 sustained, {peak_kind}", "traffic": traffic,
-                         "fwd": {"kernel": "attn_fwd_tc (cp_attn_fwd)", "achieved": round(fwd_tf, 2),
-                                 "frac": round(fwd_tf / peak_sus, 4),
-                                 "frac_of_burst": round(fwd_tf / peak_burst, 4)}},
+                         "ms_per_launch": round(dom_ms, 3),
+                         "kernels": {k: {"ms": round(t, 3), "tflops": round(fl / (t * 1e-3) / 1e12, 2),
+                                         "frac": round(fl / (t * 1e-3) / 1e12 / peak_sus, 4),
+                                         "frac_of_burst": round(fl / (t * 1e-3) / 1e12 / peak_burst, 4)}
+                                     for k, (t, fl) in kernels.items()}},
+            "fwd_frac_of_burst": round(fwd_tf / peak_burst, 4),
+            "bwd_frac_of_burst": round(bwd_tf / peak_burst, 4),
             "e2e": {"value": round((f_fwd + f_bwd) * world / (e2e_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 3)},
             "clocks": clk,

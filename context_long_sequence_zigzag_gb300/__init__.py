@@ -38,13 +38,13 @@ CP_OK, CP_ERR_INVALID_ARG, CP_ERR_UNSUPPORTED, CP_ERR_CUDA, CP_ERR_DEVICE_TIMEOU
 CP_LAYOUT_CONTIGUOUS, CP_LAYOUT_ZIGZAG = 0, 1
 CP_DT_F32, CP_DT_BF16 = 0, 1
 CP_GQA_BLOCKED, CP_GQA_INTERLEAVED = 0, 1
-CP_OP_FWD, CP_OP_BWD, CP_OP_BLOCK_FWD, CP_OP_PERMUTE = 0, 1, 2, 3
+CP_OP_FWD, CP_OP_BWD, CP_OP_BLOCK_FWD, CP_OP_PERMUTE, CP_OP_BWD_DKDV, CP_OP_BWD_DQ = 0, 1, 2, 3, 4, 5
 
 EXPORTED = [
     "cp_status_string", "cp_validate", "cp_workspace_size", "cp_shard_offsets",
     "cp_rank_block_counts", "cp_shard_permute", "cp_attn_block_fwd", "cp_lse_merge",
     "cp_attn_fwd", "cp_attn_bwd", "cp_device_status", "cp_check_bounded_wait",
-    "cp_attn_fwd_noalloc",
+    "cp_attn_fwd_noalloc", "cp_attn_bwd_prep", "cp_attn_bwd_dkdv", "cp_attn_bwd_dq",
 ]
 
 
@@ -83,6 +83,9 @@ _sigs = {
     "cp_device_status": (ctypes.c_int, [_P, ctypes.POINTER(ctypes.c_int32)]),
     "cp_check_bounded_wait": (ctypes.c_int, [ctypes.c_int64, ctypes.POINTER(ctypes.c_int32), _P]),
     "cp_attn_fwd_noalloc": (ctypes.c_int, [_DP, _P, _P, _P, _P, _P, _P]),
+    "cp_attn_bwd_prep": (ctypes.c_int, [_DP, _P, _P, _P, _P]),
+    "cp_attn_bwd_dkdv": (ctypes.c_int, [_DP, _P, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
+    "cp_attn_bwd_dq": (ctypes.c_int, [_DP, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
 }
 for _name, (_res, _args) in _sigs.items():
     _f = getattr(_lib, _name)
@@ -258,6 +261,37 @@ def cp_attn_bwd(prob: Problem, q, k, v, o, lse, dout, dq=None, dk=None, dv=None,
     _check(_lib.cp_attn_bwd(prob.ptr, _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout), _ptr(dq),
                             _ptr(dk), _ptr(dv), _ptr(ws), ws.numel(), _stream(stream)), "cp_attn_bwd")
     return dq, dk, dv
+
+
+def cp_attn_bwd_prep(prob: Problem, o, dout, dpsum=None, stream=None):
+    """D = rowsum(dout * o) per (head, row): float32 [hq, T]."""
+    d = prob.desc
+    if dpsum is None:
+        dpsum = torch.empty(d.hq, d.total_tokens, dtype=torch.float32, device=o.device)
+    _check(_lib.cp_attn_bwd_prep(prob.ptr, _ptr(o), _ptr(dout), _ptr(dpsum), _stream(stream)), "cp_attn_bwd_prep")
+    return dpsum
+
+
+def cp_attn_bwd_dkdv(prob: Problem, q, k, v, lse, dpsum, dout, dk=None, dv=None, ws=None, stream=None):
+    if dk is None:
+        dk = torch.empty_like(k)
+    if dv is None:
+        dv = torch.empty_like(v)
+    if ws is None:
+        ws = workspace(prob, CP_OP_BWD_DKDV, q.device)
+    _check(_lib.cp_attn_bwd_dkdv(prob.ptr, _ptr(q), _ptr(k), _ptr(v), _ptr(lse), _ptr(dpsum), _ptr(dout), _ptr(dk),
+                                 _ptr(dv), _ptr(ws), ws.numel(), _stream(stream)), "cp_attn_bwd_dkdv")
+    return dk, dv
+
+
+def cp_attn_bwd_dq(prob: Problem, q, k, v, lse, dpsum, dout, dq=None, ws=None, stream=None):
+    if dq is None:
+        dq = torch.empty_like(q)
+    if ws is None:
+        ws = workspace(prob, CP_OP_BWD_DQ, q.device)
+    _check(_lib.cp_attn_bwd_dq(prob.ptr, _ptr(q), _ptr(k), _ptr(v), _ptr(lse), _ptr(dpsum), _ptr(dout), _ptr(dq),
+                               _ptr(ws), ws.numel(), _stream(stream)), "cp_attn_bwd_dq")
+    return dq
 
 
 def cp_attn_fwd_noalloc(prob: Problem, q, k, v, o, lse, stream=None):

@@ -276,6 +276,44 @@ AttnArgs base_args(const cp_desc_t* d) {
   return a;
 }
 
+// Uploads the key-major plan into `ws` and launches the dK/dV kernel.
+cp_status_t run_bwd_dkdv(const cp_desc_t* d, const ShardMap& m, AttnArgs a, char* ws, size_t ws_bytes,
+                         cudaStream_t cs) {
+  Plan pb = build_bwd_plan(d, m);
+  order_by_work(pb);
+  if (ws == nullptr || (reinterpret_cast<uintptr_t>(ws) & 255) || ws_bytes < plan_bytes(pb)) return CP_ERR_WORKSPACE;
+  if (upload_plan(pb, ws, cs, &a.tiles, &a.ranges) != cudaSuccess) return CP_ERR_CUDA;
+  a.num_tiles = int32_t(pb.tiles.size());
+  a.max_ranges = pb.max_ranges;
+  const cudaError_t e = use_tc_bwd(d) ? launch_tc_bwd_dkdv(a, cs) : launch_simt_bwd_dkdv(a, d->dtype, cs);
+  return e == cudaSuccess ? CP_OK : CP_ERR_CUDA;
+}
+
+// Uploads the query-major plan into `ws` and launches the dQ kernel.
+cp_status_t run_bwd_dq(const cp_desc_t* d, const ShardMap& m, AttnArgs a, char* ws, size_t ws_bytes,
+                       cudaStream_t cs) {
+  Plan pf = build_fwd_plan(d, m, -1, -1);
+  order_by_work(pf);
+  if (ws == nullptr || (reinterpret_cast<uintptr_t>(ws) & 255) || ws_bytes < plan_bytes(pf)) return CP_ERR_WORKSPACE;
+  if (upload_plan(pf, ws, cs, &a.tiles, &a.ranges) != cudaSuccess) return CP_ERR_CUDA;
+  a.num_tiles = int32_t(pf.tiles.size());
+  a.max_ranges = pf.max_ranges;
+  const cudaError_t e = use_tc_bwd(d) ? launch_tc_bwd_dq(a, cs) : launch_simt_bwd_dq(a, d->dtype, cs);
+  return e == cudaSuccess ? CP_OK : CP_ERR_CUDA;
+}
+
+AttnArgs bwd_args(const cp_desc_t* d, const void* q, const void* k, const void* v, const float* lse,
+                  const float* dpsum, const void* dout) {
+  AttnArgs a = base_args(d);
+  a.q = q;
+  a.k = k;
+  a.v = v;
+  a.lse_in = lse;
+  a.dpsum = const_cast<float*>(dpsum);
+  a.dout = dout;
+  return a;
+}
+
 struct BwdLayout {
   size_t fwd_plan, bwd_plan, dpsum, total;
 };
@@ -364,6 +402,10 @@ cp_status_t cp_workspace_size(const cp_desc_t* d, int32_t op, size_t* bytes) {
     *bytes = mx;
   } else if (op == CP_OP_BWD) {
     *bytes = bwd_layout(d, build_fwd_plan(d, m, -1, -1), build_bwd_plan(d, m)).total;
+  } else if (op == CP_OP_BWD_DKDV) {
+    *bytes = plan_bytes(build_bwd_plan(d, m));
+  } else if (op == CP_OP_BWD_DQ) {
+    *bytes = plan_bytes(build_fwd_plan(d, m, -1, -1));
   } else {
     return CP_ERR_INVALID_ARG;
   }
@@ -518,51 +560,66 @@ cp_status_t cp_attn_bwd(const cp_desc_t* d, const void* q, const void* k, const 
   ShardMap m = build_map(d);
   Plan pf = build_fwd_plan(d, m, -1, -1);
   Plan pb = build_bwd_plan(d, m);
-  order_by_work(pf);
-  order_by_work(pb);
   BwdLayout L = bwd_layout(d, pf, pb);
   if (ws == nullptr || (reinterpret_cast<uintptr_t>(ws) & 255) || ws_bytes < L.total)
     return CP_ERR_WORKSPACE;
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
   char* base = static_cast<char*>(ws);
-  AttnArgs a = base_args(d);
-  a.q = q;
-  a.k = k;
-  a.v = v;
+  float* dpsum = reinterpret_cast<float*>(base + L.dpsum);
+  AttnArgs a = bwd_args(d, q, k, v, lse, dpsum, dout);
   a.o = o;
-  a.lse_in = lse;
+  if (launch_bwd_preprocess(a, d->dtype, cs) != cudaSuccess) return CP_ERR_CUDA;
+  AttnArgs ak = a;
+  ak.dk = dk;
+  ak.dv = dv;
+  st = run_bwd_dkdv(d, m, ak, base + L.bwd_plan, L.dpsum - L.bwd_plan, cs);
+  if (st != CP_OK) return st;
+  AttnArgs aq = a;
+  aq.dq = dq;
+  return run_bwd_dq(d, m, aq, base + L.fwd_plan, L.bwd_plan - L.fwd_plan, cs);
+}
+
+cp_status_t cp_attn_bwd_prep(const cp_desc_t* d, const void* o, const void* dout, float* dpsum, cp_stream_t stream) {
+  cp_status_t st = check_attn_fields(d);
+  if (st != CP_OK) return st;
+  if (d->total_tokens == 0) return CP_OK;
+  if (!o || !dout || !dpsum || !aligned16(o) || !aligned16(dout) || (reinterpret_cast<uintptr_t>(dpsum) & 3))
+    return CP_ERR_INVALID_ARG;
+  AttnArgs a = base_args(d);
+  a.o = o;
   a.dout = dout;
-  a.dq = dq;
+  a.dpsum = dpsum;
+  return launch_bwd_preprocess(a, d->dtype, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? CP_OK
+                                                                                                 : CP_ERR_CUDA;
+}
+
+cp_status_t cp_attn_bwd_dkdv(const cp_desc_t* d, const void* q, const void* k, const void* v, const float* lse,
+                             const float* dpsum, const void* dout, void* dk, void* dv, void* ws, size_t ws_bytes,
+                             cp_stream_t stream) {
+  cp_status_t st = check_attn_fields(d);
+  if (st != CP_OK) return st;
+  if (d->total_tokens == 0) return CP_OK;
+  const void* ptrs[] = {q, k, v, lse, dpsum, dout, dk, dv};
+  for (const void* p : ptrs)
+    if (p == nullptr || !aligned16(p)) return CP_ERR_INVALID_ARG;
+  AttnArgs a = bwd_args(d, q, k, v, lse, dpsum, dout);
   a.dk = dk;
   a.dv = dv;
-  a.dpsum = reinterpret_cast<float*>(base + L.dpsum);
+  return run_bwd_dkdv(d, build_map(d), a, static_cast<char*>(ws), ws_bytes, reinterpret_cast<cudaStream_t>(stream));
+}
 
-  if (launch_bwd_preprocess(a, d->dtype, cs) != cudaSuccess) return CP_ERR_CUDA;
-  if (use_tc_bwd(d)) {
-    // dK, dV over the key-major plan; dQ over the query-major plan
-    AttnArgs ak = a;
-    if (upload_plan(pb, base + L.bwd_plan, cs, &ak.tiles, &ak.ranges) != cudaSuccess) return CP_ERR_CUDA;
-    ak.num_tiles = int32_t(pb.tiles.size());
-    ak.max_ranges = pb.max_ranges;
-    if (launch_tc_bwd_dkdv(ak, cs) != cudaSuccess) return CP_ERR_CUDA;
-    AttnArgs aq = a;
-    if (upload_plan(pf, base + L.fwd_plan, cs, &aq.tiles, &aq.ranges) != cudaSuccess) return CP_ERR_CUDA;
-    aq.num_tiles = int32_t(pf.tiles.size());
-    aq.max_ranges = pf.max_ranges;
-    if (launch_tc_bwd_dq(aq, cs) != cudaSuccess) return CP_ERR_CUDA;
-    return CP_OK;
-  }
-  AttnArgs aq = a;
-  if (upload_plan(pf, base + L.fwd_plan, cs, &aq.tiles, &aq.ranges) != cudaSuccess) return CP_ERR_CUDA;
-  aq.num_tiles = int32_t(pf.tiles.size());
-  aq.max_ranges = pf.max_ranges;
-  if (launch_simt_bwd_dq(aq, d->dtype, cs) != cudaSuccess) return CP_ERR_CUDA;
-  AttnArgs ak = a;
-  if (upload_plan(pb, base + L.bwd_plan, cs, &ak.tiles, &ak.ranges) != cudaSuccess) return CP_ERR_CUDA;
-  ak.num_tiles = int32_t(pb.tiles.size());
-  ak.max_ranges = pb.max_ranges;
-  if (launch_simt_bwd_dkdv(ak, d->dtype, cs) != cudaSuccess) return CP_ERR_CUDA;
-  return CP_OK;
+cp_status_t cp_attn_bwd_dq(const cp_desc_t* d, const void* q, const void* k, const void* v, const float* lse,
+                           const float* dpsum, const void* dout, void* dq, void* ws, size_t ws_bytes,
+                           cp_stream_t stream) {
+  cp_status_t st = check_attn_fields(d);
+  if (st != CP_OK) return st;
+  if (d->total_tokens == 0) return CP_OK;
+  const void* ptrs[] = {q, k, v, lse, dpsum, dout, dq};
+  for (const void* p : ptrs)
+    if (p == nullptr || !aligned16(p)) return CP_ERR_INVALID_ARG;
+  AttnArgs a = bwd_args(d, q, k, v, lse, dpsum, dout);
+  a.dq = dq;
+  return run_bwd_dq(d, build_map(d), a, static_cast<char*>(ws), ws_bytes, reinterpret_cast<cudaStream_t>(stream));
 }
 
 cp_status_t cp_attn_fwd_noalloc(const cp_desc_t* d, const void* q, const void* k, const void* v, void* o,

@@ -82,7 +82,9 @@ typedef enum {
 typedef enum { CP_LAYOUT_CONTIGUOUS = 0, CP_LAYOUT_ZIGZAG = 1 } cp_layout_t;
 typedef enum { CP_DT_F32 = 0, CP_DT_BF16 = 1 } cp_dtype_t;
 typedef enum { CP_GQA_BLOCKED = 0, CP_GQA_INTERLEAVED = 1 } cp_gqa_t;
-typedef enum { CP_OP_FWD = 0, CP_OP_BWD = 1, CP_OP_BLOCK_FWD = 2, CP_OP_PERMUTE = 3 } cp_op_t;
+typedef enum {
+  CP_OP_FWD = 0, CP_OP_BWD = 1, CP_OP_BLOCK_FWD = 2, CP_OP_PERMUTE = 3, CP_OP_BWD_DKDV = 4, CP_OP_BWD_DQ = 5
+} cp_op_t;
 
 /* Problem descriptor.  Read on the host during each call; not retained. */
 typedef struct {
@@ -210,6 +212,34 @@ cp_status_t cp_attn_bwd(const cp_desc_t* desc, const void* q, const void* k, con
 #define CP_NOALLOC_SCRATCH_BYTES (4u << 20)
 cp_status_t cp_attn_fwd_noalloc(const cp_desc_t* desc, const void* q, const void* k, const void* v,
                                 void* o, float* lse, cp_stream_t stream);
+
+/* The backward in three independent pieces (cp_attn_bwd runs all three).
+ *
+ * cp_attn_bwd_prep: D = rowsum(dout * o) for every (head, row), the second
+ * statistic the recomputed backward needs besides lse
+ * ("Ulysses与Ring-Attention详解" §4.3).
+ *   o, dout : device [T, hq, d_v] (desc.dtype), sharded order
+ *   dpsum   : device float32 [hq, T]
+ * No workspace. */
+cp_status_t cp_attn_bwd_prep(const cp_desc_t* desc, const void* o, const void* dout, float* dpsum,
+                             cp_stream_t stream);
+
+/* cp_attn_bwd_dkdv: dk and dv (each summed over the query heads of its GQA
+ * group) from q, k, v, the forward's lse, dpsum (cp_attn_bwd_prep) and dout.
+ * Key-tile-major: every key tile visits the query runs of all virtual ranks
+ * that see it.  workspace: cp_workspace_size(desc, CP_OP_BWD_DKDV) bytes. */
+cp_status_t cp_attn_bwd_dkdv(const cp_desc_t* desc, const void* q, const void* k, const void* v,
+                             const float* lse, const float* dpsum, const void* dout, void* dk, void* dv,
+                             void* workspace, size_t workspace_bytes, cp_stream_t stream);
+
+/* cp_attn_bwd_dq: dq from the same inputs, query-tile-major (dq accumulates
+ * on chip over every visible key tile and is written once).
+ * workspace: cp_workspace_size(desc, CP_OP_BWD_DQ) bytes.  Independent of
+ * cp_attn_bwd_dkdv: the two may run concurrently on different streams, each
+ * with its own workspace. */
+cp_status_t cp_attn_bwd_dq(const cp_desc_t* desc, const void* q, const void* k, const void* v,
+                           const float* lse, const float* dpsum, const void* dout, void* dq,
+                           void* workspace, size_t workspace_bytes, cp_stream_t stream);
 
 /* Synchronises `stream`, then returns and clears the device error word of
  * the current device: *code = 0 when every bounded wait since the last call

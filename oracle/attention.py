@@ -155,59 +155,72 @@ def _seq_of_rows(cu: list, rows: np.ndarray) -> np.ndarray:
     return np.searchsorted(np.asarray(cu), rows, side="right") - 1
 
 
+def _rows_by_seq(cu: list, rows: np.ndarray):
+    """Groups sampled global rows by sequence: yields (a, b, positions in rows)."""
+    seq = _seq_of_rows(cu, rows)
+    for s in np.unique(seq):
+        yield cu[s], cu[s + 1], np.nonzero(seq == s)[0]
+
+
 def attn_forward_rows(q, k, v, cu_seqlens, scale: float, rows: Sequence[int],
-                      heads: Iterable[int], causal: bool = True, gqa: str = "blocked"):
+                      heads: Iterable[int], causal: bool = True, gqa: str = "blocked",
+                      chunk: int = 64):
     """Forward for selected global query rows and query heads only.
 
+    Every selected row gets the full-row softmax over its visible keys; rows
+    of one sequence are handled together as a small matrix product.
     Returns o [n_rows, n_heads, dv] and lse [n_heads, n_rows].
     """
     rows = np.asarray(rows, dtype=np.int64)
     heads = list(heads)
     hq, hkv = q.shape[1], k.shape[1]
     cu = _cu(cu_seqlens)
-    seq = _seq_of_rows(cu, rows)
     dv = v.shape[2]
     o = np.zeros((len(rows), len(heads), dv))
     lse = np.full((len(heads), len(rows)), -np.inf)
     for hi, h in enumerate(heads):
         kvh = kv_head(h, hq, hkv, gqa)
-        for ri, (i, s) in enumerate(zip(rows, seq)):
-            a, b = cu[s], cu[s + 1]
-            hi_end = i + 1 if causal else b
-            K = _f64(k[a:hi_end, kvh])
-            V = _f64(v[a:hi_end, kvh])
-            S = scale * (K @ _f64(q[i, h]))
-            P, l = _softmax_rows(S[None, :], np.ones((1, S.shape[0]), dtype=bool))
-            o[ri, hi] = P[0] @ V
-            lse[hi, ri] = l[0]
+        for a, b, idx in _rows_by_seq(cu, rows):
+            K = _f64(k[a:b, kvh])
+            V = _f64(v[a:b, kvh])
+            for c0 in range(0, len(idx), chunk):
+                sel = idx[c0:c0 + chunk]
+                pos = rows[sel] - a
+                Qs = _f64(q[rows[sel], h])
+                S = scale * (Qs @ K.T)
+                vis = (np.arange(b - a)[None, :] <= pos[:, None]) if causal else np.ones_like(S, dtype=bool)
+                P, l = _softmax_rows(S, vis)
+                o[sel, hi] = P @ V
+                lse[hi, sel] = l
     return o, lse
 
 
 def attn_backward_dq_rows(q, k, v, dout, cu_seqlens, scale: float, rows: Sequence[int],
-                          heads: Iterable[int], causal: bool = True, gqa: str = "blocked"):
+                          heads: Iterable[int], causal: bool = True, gqa: str = "blocked",
+                          chunk: int = 64):
     """dq for selected global query rows / query heads: [n_rows, n_heads, dk]."""
     rows = np.asarray(rows, dtype=np.int64)
     heads = list(heads)
     hq, hkv = q.shape[1], k.shape[1]
     cu = _cu(cu_seqlens)
-    seq = _seq_of_rows(cu, rows)
     out = np.zeros((len(rows), len(heads), q.shape[2]))
     for hi, h in enumerate(heads):
         kvh = kv_head(h, hq, hkv, gqa)
-        for ri, (i, s) in enumerate(zip(rows, seq)):
-            a, b = cu[s], cu[s + 1]
-            end = i + 1 if causal else b
-            K = _f64(k[a:end, kvh])
-            V = _f64(v[a:end, kvh])
-            qi, doi = _f64(q[i, h]), _f64(dout[i, h])
-            S = scale * (K @ qi)
-            P, _ = _softmax_rows(S[None, :], np.ones((1, S.shape[0]), dtype=bool))
-            P = P[0]
-            oi = P @ V
-            Di = doi @ oi
-            dP = V @ doi
-            dS = P * (dP - Di)
-            out[ri, hi] = scale * (dS @ K)
+        for a, b, idx in _rows_by_seq(cu, rows):
+            K = _f64(k[a:b, kvh])
+            V = _f64(v[a:b, kvh])
+            for c0 in range(0, len(idx), chunk):
+                sel = idx[c0:c0 + chunk]
+                pos = rows[sel] - a
+                Qs, dOs = _f64(q[rows[sel], h]), _f64(dout[rows[sel], h])
+                S = scale * (Qs @ K.T)
+                vis = (np.arange(b - a)[None, :] <= pos[:, None]) if causal else np.ones_like(S, dtype=bool)
+                P, _ = _softmax_rows(S, vis)
+                O = P @ V
+                Di = (dOs * O).sum(axis=1)
+                dP = dOs @ V.T
+                dS = P * (dP - Di[:, None])
+                out[sel, hi] = scale * (dS @ K)
     return out
 
 

@@ -60,6 +60,9 @@ BF16_CASES = [
     dict(total_tokens=2500, hq=4, hkv=2, d_qk=128, d_v=128, cp_size=3, layout="contiguous",
          seqlens=(1200, 9, 1291)),
     dict(total_tokens=1024, hq=2, hkv=2, d_qk=192, d_v=128, cp_size=4, layout="zigzag", sigma=0.5),
+    # MLA-shaped heads with GQA and a ragged varlen pack (64-row query steps)
+    dict(total_tokens=2000, hq=4, hkv=2, d_qk=192, d_v=128, cp_size=4, layout="zigzag", sigma=0.5,
+         seqlens=(1300, 5, 695)),
 ]
 
 
@@ -77,3 +80,26 @@ def test_bf16_backward_interleaved_gqa_noncausal():
     got, ref = _run(w, gqa="interleaved")
     for n in ("dq", "dk", "dv"):
         assert rel_fro(got[n], ref[n]) < BF16_GRAD_RFRO, n
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_split_backward_matches_combined(dtype):
+    # cp_attn_bwd_prep + cp_attn_bwd_dkdv + cp_attn_bwd_dq run the same
+    # kernels as cp_attn_bwd: results are bit-identical.
+    d = 128 if dtype == "bf16" else 64
+    w = workloads.Workload(name="t", total_tokens=1500, hq=4, hkv=2, d_qk=d, d_v=d, cp_size=4, layout="zigzag",
+                           dtype=dtype, seed=23, seqlens=(1000, 500))
+    inp = workloads.make_inputs(w, device="cuda", with_dout=True)
+    prob = cpa.Problem(w.total_tokens, w.hq, w.hkv, d, d, 4, "zigzag", inp["cu_seqlens"].tolist(), True, w.scale,
+                       "blocked", torch.float32 if dtype == "f32" else torch.bfloat16)
+    q, k, v, do = (inp[n] for n in ("q", "k", "v", "dout"))
+    o, lse = cpa.cp_attn_fwd(prob, q, k, v)
+    dq, dk, dv = cpa.cp_attn_bwd(prob, q, k, v, o, lse, do)
+    dps = cpa.cp_attn_bwd_prep(prob, o, do)
+    dk2, dv2 = cpa.cp_attn_bwd_dkdv(prob, q, k, v, lse, dps, do)
+    dq2 = cpa.cp_attn_bwd_dq(prob, q, k, v, lse, dps, do)
+    torch.cuda.synchronize()
+    assert torch.equal(dq, dq2) and torch.equal(dk, dk2) and torch.equal(dv, dv2)
+    # D itself: rowsum(dout * o) in float64 from the same bf16/f32 tensors
+    want = (do.double() * o.double()).sum(-1).transpose(0, 1)
+    assert float((dps.double() - want).abs().max()) < 1e-3
