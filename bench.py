@@ -258,6 +258,46 @@ def e2e_measure(r: Runner, steps: int, warmup: int):
     return e0.elapsed_time(e1) / steps, h2d, d2h
 
 
+def aux_bandwidth(r: "Runner", reps: int = 5) -> dict:
+    """HBM throughput of the bandwidth-bound kernels on buffers larger than L2:
+    the shard permutation of q (one launch) and one LSE merge of fp32
+    partials over all rows and heads (the stepwise ring's update)."""
+    cpa, w, dev = r.cpa, r.w, r.dev
+    out = {}
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+    x = r.g["q"]
+    y = torch.empty_like(x)
+    nbytes = 2 * x.numel() * x.element_size()
+    times = []
+    for i in range(reps + 1):
+        ev[0].record()
+        cpa.cp_shard_permute(r.prob, x, out=y, ws=r.ws_perm)
+        ev[1].record()
+        torch.cuda.synchronize()
+        if i:
+            times.append(ev[0].elapsed_time(ev[1]))
+    out["shard_permute"] = {"bytes": nbytes, "ms": round(min(times), 4),
+                            "gbs": round(nbytes / (min(times) * 1e-3) / 1e9, 1)}
+    rows = w.total_tokens
+    o_acc = torch.randn(rows, w.hq, w.d_v, device=dev)
+    o_part = torch.randn(rows, w.hq, w.d_v, device=dev)
+    l_acc = torch.randn(w.hq, rows, device=dev)
+    l_part = torch.randn(w.hq, rows, device=dev)
+    nbytes = rows * w.hq * (3 * w.d_v * 4 + 12)
+    times = []
+    for i in range(reps + 1):
+        ev[0].record()
+        cpa.cp_lse_merge(r.prob, o_acc, l_acc, o_part, l_part)
+        ev[1].record()
+        torch.cuda.synchronize()
+        if i:
+            times.append(ev[0].elapsed_time(ev[1]))
+    out["lse_merge"] = {"bytes": nbytes, "ms": round(min(times), 4),
+                        "gbs": round(nbytes / (min(times) * 1e-3) / 1e9, 1)}
+    del o_acc, o_part, l_acc, l_part, y
+    return out
+
+
 def run_gpu(args):
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -306,6 +346,7 @@ def run_gpu(args):
     fwd_ms, bwd_ms, dkdv_ms, dq_ms = r.kernel_times_ms()
 
     e2e_ms, h2d, d2h = e2e_measure(r, max(1, min(args.steps, 3)), 1)
+    aux = aux_bandwidth(r)
 
     peaks, peak_kind = load_peaks()
     peak_sus = float(peaks.get("bf16_tflops_sustained", FALLBACK["bf16_tflops_sustained"]))
@@ -356,6 +397,9 @@ def run_gpu(args):
                                          "frac": round(fl / (t * 1e-3) / 1e12 / peak_sus, 4),
                                          "frac_of_burst": round(fl / (t * 1e-3) / 1e12 / peak_burst, 4)}
                                      for k, (t, fl) in kernels.items()}},
+            "hbm_kernels": {k: dict(v, frac=round(v["gbs"] / float(peaks.get("hbm_gbs", FALLBACK["hbm_gbs"])), 4),
+                                    peak_gbs=float(peaks.get("hbm_gbs", FALLBACK["hbm_gbs"])))
+                            for k, v in aux.items()},
             "fwd_frac_of_burst": round(fwd_tf / peak_burst, 4),
             "bwd_frac_of_burst": round(bwd_tf / peak_burst, 4),
             "e2e": {"value": round((f_fwd + f_bwd) * world / (e2e_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
