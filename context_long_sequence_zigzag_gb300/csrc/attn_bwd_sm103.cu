@@ -326,8 +326,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dkdv_kernel(const __grid
       }
     }
   } else if (warp == 9) {
-    // ------------------------------------------------------------ MMA issuer
-    if (lane == 0 && n_steps > 0) {
+    // ------------------------------------------------------------ MMA issuer (whole warp)
+    if (n_steps > 0) {
       constexpr uint32_t idS = ptx::idesc_bf16_f32(BT, BNQ, false, false);
       constexpr uint32_t idDV = ptx::idesc_bf16_f32(BT, DV, false, true);  // B = dO, MN-major
       constexpr uint32_t idDK = ptx::idesc_bf16_f32(BT, DQK, false, true);  // B = Q, MN-major
@@ -340,7 +340,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dkdv_kernel(const __grid
         const uint64_t da = ptx::sdesc_sw128(abase, 16, 1024), db = ptx::sdesc_sw128(bbase, 16, 1024);
 #pragma unroll
         for (int kk = 0; kk < ksteps; ++kk)
-          ptx::mma_ss(d, da + (((kk >> 2) * kPanel + (kk & 3) * 32) >> 4),
+          ptx::mma_ss_w(d, da + (((kk >> 2) * kPanel + (kk & 3) * 32) >> 4),
                       db + (((kk >> 2) * Cfg::kQPanel + (kk & 3) * 32) >> 4), idS, kk > 0);
       };
       // D += (packed bf16 A in TMEM: group 0 at a0, group 1 at a0 + kPk1) x B (MN-major smem)
@@ -349,52 +349,52 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dkdv_kernel(const __grid
 #pragma unroll
         for (int kk = 0; kk < BNQ / 16; ++kk) {
           const uint32_t acol = kk < BNQ / 32 ? kk * 8 : Cfg::kPk1 + (kk - BNQ / 32) * 8;
-          ptx::mma_ts(d, a0 + acol, db + ((kk * 2048) >> 4), idesc, (acc || kk > 0));
+          ptx::mma_ts_w(d, a0 + acol, db + ((kk * 2048) >> 4), idesc, (acc || kk > 0));
         }
       };
-      bool ok = ptx::mbar_wait(bar_kv, 0, kSiteKV, wctx) && ptx::mbar_wait(bar_q_full(0), 0, kSiteQFull, wctx);
+      bool ok = ptx::mbar_wait_w(bar_kv, 0, kSiteKV, wctx) && ptx::mbar_wait_w(bar_q_full(0), 0, kSiteQFull, wctx);
       if (ok) {
         ptx::tc_fence_after();
         issue_ss(tS, kb, qb(0), DQK / 16);
-        ptx::mma_commit(bar_s_full);
+        ptx::mma_commit_w(bar_s_full);
       }
       for (int i = 0; ok && i < n_steps; ++i) {
         // dK(i-1) needs dS(i-1): once it is issued, dP(i) may overwrite tDP
         if (i > 0) {
-          if (!ptx::mbar_wait(bar_ds_full, (i - 1) & 1, kSiteDSFull, wctx)) { ok = false; break; }
+          if (!ptx::mbar_wait_w(bar_ds_full, (i - 1) & 1, kSiteDSFull, wctx)) { ok = false; break; }
           ptx::tc_fence_after();
           issue_ts(tDK, tDP, qb(i - 1), idDK, i - 1 > 0);
-          ptx::mma_commit(bar_q_empty((i - 1) % Cfg::NS));
+          ptx::mma_commit_w(bar_q_empty((i - 1) % Cfg::NS));
         }
         issue_ss(tDP, vb, ob(i), DV / 16);
-        ptx::mma_commit(bar_dp_full);
+        ptx::mma_commit_w(bar_dp_full);
         // dV(i) needs P(i); once it is issued, S(i+1) may overwrite tS
-        if (!ptx::mbar_wait(bar_p_full, i & 1, kSitePFull, wctx)) { ok = false; break; }
+        if (!ptx::mbar_wait_w(bar_p_full, i & 1, kSitePFull, wctx)) { ok = false; break; }
         ptx::tc_fence_after();
         issue_ts(tDV, tS, ob(i), idDV, i > 0);
         if (i + 1 < n_steps) {
-          if (!ptx::mbar_wait(bar_q_full((i + 1) % Cfg::NS), ((i + 1) / Cfg::NS) & 1, kSiteQFull, wctx)) {
+          if (!ptx::mbar_wait_w(bar_q_full((i + 1) % Cfg::NS), ((i + 1) / Cfg::NS) & 1, kSiteQFull, wctx)) {
             ok = false;
             break;
           }
           ptx::tc_fence_after();
           issue_ss(tS, kb, qb(i + 1), DQK / 16);
-          ptx::mma_commit(bar_s_full);
+          ptx::mma_commit_w(bar_s_full);
         }
       }
       if (ok) {
-        ok = ptx::mbar_wait(bar_ds_full, (n_steps - 1) & 1, kSiteDSFull, wctx);
+        ok = ptx::mbar_wait_w(bar_ds_full, (n_steps - 1) & 1, kSiteDSFull, wctx);
         if (ok) {
           ptx::tc_fence_after();
           issue_ts(tDK, tDP, qb(n_steps - 1), idDK, n_steps - 1 > 0);
-          ptx::mma_commit(bar_final);
+          ptx::mma_commit_w(bar_final);
         }
       }
       if (!ok) {
         volatile int no_abort = 0;
         const ptx::WaitCtx drain{&no_abort, nullptr, kWaitLimitNs};
-        ptx::mma_commit(bar_drain);
-        ptx::mbar_wait(bar_drain, 0, kSiteDrain, drain);
+        ptx::mma_commit_w(bar_drain);
+        ptx::mbar_wait_w(bar_drain, 0, kSiteDrain, drain);
       }
     }
   } else {
@@ -664,8 +664,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dq_kernel(const __grid_c
       }
     }
   } else if (warp == 9) {
-    // ------------------------------------------------------------ MMA issuer
-    if (lane == 0 && n_kv > 0) {
+    // ------------------------------------------------------------ MMA issuer (whole warp)
+    if (n_kv > 0) {
       constexpr uint32_t idS = ptx::idesc_bf16_f32(BT, BT, false, false);
       constexpr uint32_t idQ = ptx::idesc_bf16_f32(BT, DQK, false, true);  // dQ: B = K as MN-major
       const uint32_t tS = tmem + Cfg::tS, tDP = tmem + Cfg::tDP, tDQ = tmem + Cfg::tDQ;
@@ -677,61 +677,61 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dq_kernel(const __grid_c
 #pragma unroll
         for (int kk = 0; kk < ksteps; ++kk) {
           const uint32_t off = ((kk >> 2) * kPanel + (kk & 3) * 32) >> 4;
-          ptx::mma_ss(d, da + off, db + off, idS, kk > 0);
+          ptx::mma_ss_w(d, da + off, db + off, idS, kk > 0);
         }
       };
-      bool ok = ptx::mbar_wait(bar_q, 0, kSiteQ, wctx) && ptx::mbar_wait(bar_k_full(0), 0, kSiteKVFull, wctx);
+      bool ok = ptx::mbar_wait_w(bar_q, 0, kSiteQ, wctx) && ptx::mbar_wait_w(bar_k_full(0), 0, kSiteKVFull, wctx);
       if (ok) {
         ptx::tc_fence_after();
         issue_ss(tS, qb, kb(0), DQK / 16);
-        ptx::mma_commit(bar_s_full);
-        ok = ptx::mbar_wait(bar_v_full(0), 0, kSiteKVFull, wctx);
+        ptx::mma_commit_w(bar_s_full);
+        ok = ptx::mbar_wait_w(bar_v_full(0), 0, kSiteKVFull, wctx);
       }
       if (ok) {
         ptx::tc_fence_after();
         issue_ss(tDP, obb, vb(0), DV / 16);
-        ptx::mma_commit(bar_dp_full);
-        ptx::mma_commit(bar_v_empty(0));
+        ptx::mma_commit_w(bar_dp_full);
+        ptx::mma_commit_w(bar_v_empty(0));
       }
       for (int j = 0; ok && j < n_kv; ++j) {
         if (j + 1 < n_kv) {
           // S(j+1) as soon as the compute warps have read S(j)
-          if (!ptx::mbar_wait(bar_p_full, j & 1, kSitePFull, wctx) ||
-              !ptx::mbar_wait(bar_k_full((j + 1) % Cfg::NSK), ((j + 1) / Cfg::NSK) & 1, kSiteKVFull, wctx)) {
+          if (!ptx::mbar_wait_w(bar_p_full, j & 1, kSitePFull, wctx) ||
+              !ptx::mbar_wait_w(bar_k_full((j + 1) % Cfg::NSK), ((j + 1) / Cfg::NSK) & 1, kSiteKVFull, wctx)) {
             ok = false;
             break;
           }
           ptx::tc_fence_after();
           issue_ss(tS, qb, kb(j + 1), DQK / 16);
-          ptx::mma_commit(bar_s_full);
+          ptx::mma_commit_w(bar_s_full);
           // dP(j+1) as soon as they have read dP(j)
-          if (!ptx::mbar_wait(bar_dp_read, j & 1, kSiteDPFull, wctx) ||
-              !ptx::mbar_wait(bar_v_full((j + 1) % Cfg::NSV), ((j + 1) / Cfg::NSV) & 1, kSiteKVFull, wctx)) {
+          if (!ptx::mbar_wait_w(bar_dp_read, j & 1, kSiteDPFull, wctx) ||
+              !ptx::mbar_wait_w(bar_v_full((j + 1) % Cfg::NSV), ((j + 1) / Cfg::NSV) & 1, kSiteKVFull, wctx)) {
             ok = false;
             break;
           }
           ptx::tc_fence_after();
           issue_ss(tDP, obb, vb(j + 1), DV / 16);
-          ptx::mma_commit(bar_dp_full);
-          ptx::mma_commit(bar_v_empty((j + 1) % Cfg::NSV));
+          ptx::mma_commit_w(bar_dp_full);
+          ptx::mma_commit_w(bar_v_empty((j + 1) % Cfg::NSV));
         }
         // dQ(j) += dS(j) K(j), dS(j) in buffer j % NB
-        if (!ptx::mbar_wait(bar_ds_full, j & 1, kSiteDSFull, wctx)) { ok = false; break; }
+        if (!ptx::mbar_wait_w(bar_ds_full, j & 1, kSiteDSFull, wctx)) { ok = false; break; }
         ptx::tc_fence_after();
         const uint64_t kd = ptx::sdesc_sw128(kb(j), kPanel, 1024);
         const uint32_t tA = tmem + Cfg::tDS + 64 * (j % NB);
 #pragma unroll
         for (int kk = 0; kk < BT / 16; ++kk)
-          ptx::mma_ts(tDQ, tA + kk * 8, kd + ((kk * 2048) >> 4), idQ, (j > 0 || kk > 0));
-        ptx::mma_commit(bar_dq_done(j % NB));
-        ptx::mma_commit(bar_k_empty(j % Cfg::NSK));
+          ptx::mma_ts_w(tDQ, tA + kk * 8, kd + ((kk * 2048) >> 4), idQ, (j > 0 || kk > 0));
+        ptx::mma_commit_w(bar_dq_done(j % NB));
+        ptx::mma_commit_w(bar_k_empty(j % Cfg::NSK));
       }
-      if (ok) ptx::mma_commit(bar_final);
+      if (ok) ptx::mma_commit_w(bar_final);
       if (!ok) {
         volatile int no_abort = 0;
         const ptx::WaitCtx drain{&no_abort, nullptr, kWaitLimitNs};
-        ptx::mma_commit(bar_drain);
-        ptx::mbar_wait(bar_drain, 0, kSiteDrain, drain);
+        ptx::mma_commit_w(bar_drain);
+        ptx::mbar_wait_w(bar_drain, 0, kSiteDrain, drain);
       }
     }
   } else {

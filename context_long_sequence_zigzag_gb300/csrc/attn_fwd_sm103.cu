@@ -207,8 +207,8 @@ __global__ void __launch_bounds__(192, 1) attn_fwd_tc_kernel(const __grid_consta
       }
     }
   } else if (warp == 5) {
-    // ------------------------------------------------------------ MMA issuer
-    if (lane == 0 && n_kv > 0) {
+    // ------------------------------------------------------------ MMA issuer (whole warp)
+    if (n_kv > 0) {
       constexpr uint32_t idS = ptx::idesc_bf16_f32(BM, BN, false, false);
       constexpr uint32_t idO = ptx::idesc_bf16_f32(BM, DV, false, true);
       const uint32_t tO = tmem + Cfg::tO;
@@ -219,17 +219,17 @@ __global__ void __launch_bounds__(192, 1) attn_fwd_tc_kernel(const __grid_consta
         const uint32_t tS = tmem + Cfg::tS0 + BN * (j & 1);
 #pragma unroll
         for (int kk = 0; kk < DQK / 16; ++kk)
-          ptx::mma_ts(tS, tmem + Cfg::tQ + kk * 8, kd + (((kk >> 2) * kSubTile + (kk & 3) * 32) >> 4), idS, kk > 0);
-        ptx::mma_commit(bar_s_full(j & 1));
-        ptx::mma_commit(bar_k_empty(sk));
+          ptx::mma_ts_w(tS, tmem + Cfg::tQ + kk * 8, kd + (((kk >> 2) * kSubTile + (kk & 3) * 32) >> 4), idS, kk > 0);
+        ptx::mma_commit_w(bar_s_full(j & 1));
+        ptx::mma_commit_w(bar_k_empty(sk));
       };
-      bool ok = ptx::mbar_wait(bar_q, 0, kSiteQ, wctx) && ptx::mbar_wait(bar_k_full(0), 0, kSiteKFull, wctx);
+      bool ok = ptx::mbar_wait_w(bar_q, 0, kSiteQ, wctx) && ptx::mbar_wait_w(bar_k_full(0), 0, kSiteKFull, wctx);
       if (ok) {
         ptx::tc_fence_after();
         issue_s(0);
       }
       if (ok && n_kv > 1) {
-        ok = ptx::mbar_wait(bar_k_full(1 % Cfg::NSK), (1 / Cfg::NSK) & 1, kSiteKFull, wctx);
+        ok = ptx::mbar_wait_w(bar_k_full(1 % Cfg::NSK), (1 / Cfg::NSK) & 1, kSiteKFull, wctx);
         if (ok) {
           ptx::tc_fence_after();
           issue_s(1);
@@ -237,8 +237,8 @@ __global__ void __launch_bounds__(192, 1) attn_fwd_tc_kernel(const __grid_consta
       }
       for (int j = 0; ok && j < n_kv; ++j) {
         const int sv = j % Cfg::NSV;
-        ok = ptx::mbar_wait(bar_p_full, j & 1, kSitePFull, wctx) &&
-             ptx::mbar_wait(bar_v_full(sv), (j / Cfg::NSV) & 1, kSiteVFull, wctx);
+        ok = ptx::mbar_wait_w(bar_p_full, j & 1, kSitePFull, wctx) &&
+             ptx::mbar_wait_w(bar_v_full(sv), (j / Cfg::NSV) & 1, kSiteVFull, wctx);
         if (!ok) break;
         ptx::tc_fence_after();
         // O += P(j) V(j), P(j) over the first half of S buffer j & 1
@@ -246,12 +246,12 @@ __global__ void __launch_bounds__(192, 1) attn_fwd_tc_kernel(const __grid_consta
         const uint32_t tP = tmem + Cfg::tS0 + BN * (j & 1);
 #pragma unroll
         for (int kk = 0; kk < BN / 16; ++kk)
-          ptx::mma_ts(tO, tP + kk * 8, vd + ((kk * 2048) >> 4), idO, (j > 0 || kk > 0));
-        ptx::mma_commit(bar_o_done);
-        ptx::mma_commit(bar_v_empty(sv));
+          ptx::mma_ts_w(tO, tP + kk * 8, vd + ((kk * 2048) >> 4), idO, (j > 0 || kk > 0));
+        ptx::mma_commit_w(bar_o_done);
+        ptx::mma_commit_w(bar_v_empty(sv));
         // S(j+2) reuses buffer j & 1 once PV(j) has been issued
         if (j + 2 < n_kv) {
-          ok = ptx::mbar_wait(bar_k_full((j + 2) % Cfg::NSK), ((j + 2) / Cfg::NSK) & 1, kSiteKFull, wctx);
+          ok = ptx::mbar_wait_w(bar_k_full((j + 2) % Cfg::NSK), ((j + 2) / Cfg::NSK) & 1, kSiteKFull, wctx);
           if (!ok) break;
           ptx::tc_fence_after();
           issue_s(j + 2);
@@ -261,8 +261,8 @@ __global__ void __launch_bounds__(192, 1) attn_fwd_tc_kernel(const __grid_consta
         // Wait for every MMA already issued before TMEM is released.
         volatile int no_abort = 0;
         const ptx::WaitCtx drain{&no_abort, nullptr, kWaitLimitNs};
-        ptx::mma_commit(bar_drain);
-        ptx::mbar_wait(bar_drain, 0, kSiteDrain, drain);
+        ptx::mma_commit_w(bar_drain);
+        ptx::mbar_wait_w(bar_drain, 0, kSiteDrain, drain);
       }
     }
   } else {
@@ -320,7 +320,11 @@ __global__ void __launch_bounds__(192, 1) attn_fwd_tc_kernel(const __grid_consta
       const int kn = cur.n(), kp = cur.pos();
       int lim = row_ok ? kn : 0;
       if (a.causal) lim = min(lim, qpos - kp + 1);
-      float mx = -INFINITY;
+      // row maximum over 8 independent chains (one warp per SMSP: the
+      // latency of a single 128-long dependent chain would dominate)
+      float m8[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) m8[e] = -INFINITY;
       if (lim < BN) {
 #pragma unroll
         for (int c = 0; c < 4; ++c)
@@ -328,14 +332,16 @@ __global__ void __launch_bounds__(192, 1) attn_fwd_tc_kernel(const __grid_consta
           for (int i = 0; i < 32; ++i) {
             const float s = c * 32 + i < lim ? __uint_as_float(sr[c][i]) : -INFINITY;
             sr[c][i] = __float_as_uint(s);
-            mx = fmaxf(mx, s);
+            m8[i & 7] = fmaxf(m8[i & 7], s);
           }
       } else {
 #pragma unroll
         for (int c = 0; c < 4; ++c)
 #pragma unroll
-          for (int i = 0; i < 32; ++i) mx = fmaxf(mx, __uint_as_float(sr[c][i]));
+          for (int i = 0; i < 32; ++i) m8[i & 7] = fmaxf(m8[i & 7], __uint_as_float(sr[c][i]));
       }
+      const float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
+                             fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
       const float m_new = mx * sl2;
       float alpha = 1.f;
       if (m_new > m_ref + kRescaleThreshold) {
@@ -343,7 +349,9 @@ __global__ void __launch_bounds__(192, 1) attn_fwd_tc_kernel(const __grid_consta
         m_ref = m_new;
       }
       const float mref = m_ref == -INFINITY ? 0.f : m_ref;
-      float rs = 0.f;
+      float r8[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) r8[e] = 0.f;
       // P = exp2(s * scale * log2e - m_ref) (bf16, two per column) over the
       // first half of the S buffer; PV(j-2) read it before S(j) was issued
 #pragma unroll
@@ -353,11 +361,13 @@ __global__ void __launch_bounds__(192, 1) attn_fwd_tc_kernel(const __grid_consta
         for (int i = 0; i < 16; ++i) {
           const float e0 = ptx::ex2(fmaf(__uint_as_float(sr[c][2 * i]), sl2, -mref));
           const float e1 = ptx::ex2(fmaf(__uint_as_float(sr[c][2 * i + 1]), sl2, -mref));
-          rs += e0 + e1;
+          r8[(2 * i) & 7] += e0;
+          r8[(2 * i + 1) & 7] += e1;
           pk[i] = ptx::pack_bf16(e0, e1);
         }
         ptx::tmem_st16(tS + c * 16, pk);
       }
+      const float rs = ((r8[0] + r8[1]) + (r8[2] + r8[3])) + ((r8[4] + r8[5]) + (r8[6] + r8[7]));
       l = l * alpha + rs;
       // O may be rescaled once PV(j-1) is complete (rare: the reference
       // maximum only moves when a row's maximum grows by more than 2^8)

@@ -262,5 +262,31 @@ __device__ __forceinline__ bool elect_one_sync() {
   return pred != 0;
 }
 
+// ---------------------------------------------------------------- warp-collective MMA issue
+// The whole (converged) warp executes these; one lane, elected anew for
+// every instruction, issues it.  Measured on GB300 with the pipe idle, an
+// N = 128 MMA issued this way costs the issuing warp about 24 cycles, against
+// about 44 when lane 0 alone runs the issue loop in a diverged warp; an N = 128
+// MMA executes in 64 cycles and the pipe queues only a few instructions, so
+// the issuing warp's own cost decides how much of the tensor pipe it keeps
+// busy.  Always elect.sync picks the lowest active lane, so every MMA and
+// commit of a converged warp comes from the same thread, as tcgen05.commit
+// requires.
+__device__ __forceinline__ void mma_ss_w(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                        uint32_t accumulate) {
+  if (elect_one_sync()) mma_ss(d_tmem, a_desc, b_desc, idesc, accumulate);
+}
+__device__ __forceinline__ void mma_ts_w(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                        uint32_t accumulate) {
+  if (elect_one_sync()) mma_ts(d_tmem, a_tmem, b_desc, idesc, accumulate);
+}
+__device__ __forceinline__ void mma_commit_w(uint32_t bar) {
+  if (elect_one_sync()) mma_commit(bar);
+}
+// Bounded wait of a whole warp with a warp-uniform result.
+__device__ __forceinline__ bool mbar_wait_w(uint32_t bar, uint32_t parity, int site, const WaitCtx& ctx) {
+  return __all_sync(0xffffffffu, mbar_wait(bar, parity, site, ctx));
+}
+
 }  // namespace ptx
 }  // namespace cpattn
