@@ -440,16 +440,27 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dkdv_kernel(const __grid
       uint32_t x[NC / 32][32];
       ldcols<NC>(tS + colS, x);
       float pf[NC];
+      // Warp-uniform split: only tiles on the diagonal or at a ragged edge
+      // pay for the per-element visibility test.
+      if (need_mask) {
 #pragma unroll
-      for (int j = 0; j < NC; j += 4) {
-        const float4 l4 = *reinterpret_cast<const float4*>(sL + colS + j);
-        const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+        for (int j = 0; j < NC; j += 4) {
+          const float4 l4 = *reinterpret_cast<const float4*>(sL + colS + j);
+          const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int c = j + e;
-          float pv = ptx::ex2(fmaf(colv<NC>(x, c), sl2, -lv[e]));
-          if (need_mask) pv = (c >= cmin && c < cmax) ? pv : 0.f;
-          pf[c] = pv;
+          for (int e = 0; e < 4; ++e) {
+            const int c = j + e;
+            const float pv = ptx::ex2(fmaf(colv<NC>(x, c), sl2, -lv[e]));
+            pf[c] = (c >= cmin && c < cmax) ? pv : 0.f;
+          }
+        }
+      } else {
+#pragma unroll
+        for (int j = 0; j < NC; j += 4) {
+          const float4 l4 = *reinterpret_cast<const float4*>(sL + colS + j);
+          const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) pf[j + e] = ptx::ex2(fmaf(colv<NC>(x, j + e), sl2, -lv[e]));
         }
       }
       st_bf16<NC>(tS + colPk, pf);
@@ -766,11 +777,15 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dq_kernel(const __grid_c
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(bar_p_full);  // S(j) has been read
       float pf[64];
+      if (need_mask) {  // warp-uniform: diagonal and ragged tiles only
 #pragma unroll
-      for (int c = 0; c < 64; ++c) {
-        float pv = ptx::ex2(fmaf(colv<64>(x, c), sl2, -lse2));
-        if (need_mask) pv = c < lim ? pv : 0.f;
-        pf[c] = pv;
+        for (int c = 0; c < 64; ++c) {
+          const float pv = ptx::ex2(fmaf(colv<64>(x, c), sl2, -lse2));
+          pf[c] = c < lim ? pv : 0.f;
+        }
+      } else {
+#pragma unroll
+        for (int c = 0; c < 64; ++c) pf[c] = ptx::ex2(fmaf(colv<64>(x, c), sl2, -lse2));
       }
       // ---- dS = P (dP - D) * scale
       if (!__all_sync(0xffffffffu, ptx::mbar_wait(bar_dp_full, j & 1, kSiteDPFull, wctx))) { ok = false; break; }
