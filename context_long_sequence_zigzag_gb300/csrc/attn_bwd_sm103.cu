@@ -37,9 +37,11 @@
 //
 // In both kernels two groups of four compute warps split the N columns
 // (group g owns the g-th half, thread = TMEM lane); each group writes its
-// bf16 result only into TMEM columns it has already read.  Roles (320
-// threads): warps 0-7 compute, warp 8 TMA producer, warp 9 TMEM allocator +
-// MMA issuer.
+// bf16 result only into TMEM columns it has already read.  Roles: warps 0-7
+// compute, warp 8 TMA producer, warp 9 TMEM allocator + MMA issuer; the dQ
+// kernel adds warp 10, which issues the dQ MMAs so that waiting for dS never
+// delays S and dP of the next key tile.  MMA-issuing warps run converged and
+// elect one lane per instruction.
 #include <cuda.h>
 #include <cuda_bf16.h>
 
@@ -60,6 +62,7 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 constexpr int kComputeThreads = 256;
 constexpr int kThreads = kComputeThreads + 64;
+constexpr int kThreadsDq = kComputeThreads + 96;  // dQ kernel: a second MMA-issuing warp
 
 enum WaitSite : int {
   kSiteKV = 0x21, kSiteQEmpty, kSiteQFull, kSiteSFull, kSiteDPFull, kSitePFull, kSiteDSFull, kSiteFinal,
@@ -558,7 +561,7 @@ struct DqCfg {
   static constexpr uint32_t offK = offO + kVBytes;           // NSK stages
   static constexpr uint32_t offV = offK + NSK * kKBytes;     // NSV stages
   static constexpr uint32_t offBar = offV + NSV * kVBytes;
-  static constexpr int kNumBars = 1 + 2 * NSK + 2 * NSV + 7 + NB;
+  static constexpr int kNumBars = 1 + 2 * NSK + 2 * NSV + 8 + NB;
   static constexpr uint32_t kSmem = offBar + kNumBars * 8 + 16;
   // TMEM columns
   static constexpr uint32_t tS = 0, tDP = 128, tDQ = 256, tDS = 256 + DQK;
@@ -567,7 +570,7 @@ struct DqCfg {
 };
 
 template <int DQK>
-__global__ void __launch_bounds__(kThreads, 1) attn_bwd_dq_kernel(const __grid_constant__ BwdParams p) {
+__global__ void __launch_bounds__(kThreadsDq, 1) attn_bwd_dq_kernel(const __grid_constant__ BwdParams p) {
   using Cfg = DqCfg<DQK>;
   constexpr int NB = Cfg::NB;
   extern __shared__ __align__(1024) uint8_t smem[];
@@ -598,6 +601,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dq_kernel(const __grid_c
   const uint32_t bar_drain = bar_s_full + 40;
   const uint32_t bar_dp_read = bar_s_full + 48;                        // compute warps hold dP(j)
   auto bar_dq_done = [&](int b) { return bar_s_full + 56 + 8u * b; };  // dQ(j) read dS buffer b = j % NB
+  const uint32_t bar_drain2 = bar_s_full + 56 + 8u * NB;            // drain of the dQ issuer
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Cfg::offBar + Cfg::kNumBars * 8);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Cfg::offBar + Cfg::kNumBars * 8 + 4);
 
@@ -619,6 +623,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dq_kernel(const __grid_c
     ptx::mbar_init(bar_drain, 1);
     ptx::mbar_init(bar_dp_read, 8);
     for (int b = 0; b < NB; ++b) ptx::mbar_init(bar_dq_done(b), 1);
+    ptx::mbar_init(bar_drain2, 1);
     *abort_flag = 0;
     ptx::fence_barrier_init();
   }
@@ -675,11 +680,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dq_kernel(const __grid_c
       }
     }
   } else if (warp == 9) {
-    // ------------------------------------------------------------ MMA issuer (whole warp)
+    // ------------------------------------------------------------ MMA issuer of S and dP (whole warp)
     if (n_kv > 0) {
       constexpr uint32_t idS = ptx::idesc_bf16_f32(BT, BT, false, false);
-      constexpr uint32_t idQ = ptx::idesc_bf16_f32(BT, DQK, false, true);  // dQ: B = K as MN-major
-      const uint32_t tS = tmem + Cfg::tS, tDP = tmem + Cfg::tDP, tDQ = tmem + Cfg::tDQ;
+      const uint32_t tS = tmem + Cfg::tS, tDP = tmem + Cfg::tDP;
       const uint32_t qb = sbase + Cfg::offQ, obb = sbase + Cfg::offO;
       auto kb = [&](int j) { return sbase + Cfg::offK + (j % Cfg::NSK) * Cfg::kKBytes; };
       auto vb = [&](int j) { return sbase + Cfg::offV + (j % Cfg::NSV) * Cfg::kVBytes; };
@@ -704,32 +708,50 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dq_kernel(const __grid_c
         ptx::mma_commit_w(bar_dp_full);
         ptx::mma_commit_w(bar_v_empty(0));
       }
-      for (int j = 0; ok && j < n_kv; ++j) {
-        if (j + 1 < n_kv) {
-          // S(j+1) as soon as the compute warps have read S(j)
-          if (!ptx::mbar_wait_w(bar_p_full, j & 1, kSitePFull, wctx) ||
-              !ptx::mbar_wait_w(bar_k_full((j + 1) % Cfg::NSK), ((j + 1) / Cfg::NSK) & 1, kSiteKVFull, wctx)) {
-            ok = false;
-            break;
-          }
-          ptx::tc_fence_after();
-          issue_ss(tS, qb, kb(j + 1), DQK / 16);
-          ptx::mma_commit_w(bar_s_full);
-          // dP(j+1) as soon as they have read dP(j)
-          if (!ptx::mbar_wait_w(bar_dp_read, j & 1, kSiteDPFull, wctx) ||
-              !ptx::mbar_wait_w(bar_v_full((j + 1) % Cfg::NSV), ((j + 1) / Cfg::NSV) & 1, kSiteKVFull, wctx)) {
-            ok = false;
-            break;
-          }
-          ptx::tc_fence_after();
-          issue_ss(tDP, obb, vb(j + 1), DV / 16);
-          ptx::mma_commit_w(bar_dp_full);
-          ptx::mma_commit_w(bar_v_empty((j + 1) % Cfg::NSV));
+      for (int j = 0; ok && j + 1 < n_kv; ++j) {
+        // S(j+1) as soon as the compute warps have read S(j)
+        if (!ptx::mbar_wait_w(bar_p_full, j & 1, kSitePFull, wctx) ||
+            !ptx::mbar_wait_w(bar_k_full((j + 1) % Cfg::NSK), ((j + 1) / Cfg::NSK) & 1, kSiteKVFull, wctx)) {
+          ok = false;
+          break;
         }
+        ptx::tc_fence_after();
+        issue_ss(tS, qb, kb(j + 1), DQK / 16);
+        ptx::mma_commit_w(bar_s_full);
+        // dP(j+1) as soon as they have read dP(j)
+        if (!ptx::mbar_wait_w(bar_dp_read, j & 1, kSiteDPFull, wctx) ||
+            !ptx::mbar_wait_w(bar_v_full((j + 1) % Cfg::NSV), ((j + 1) / Cfg::NSV) & 1, kSiteKVFull, wctx)) {
+          ok = false;
+          break;
+        }
+        ptx::tc_fence_after();
+        issue_ss(tDP, obb, vb(j + 1), DV / 16);
+        ptx::mma_commit_w(bar_dp_full);
+        ptx::mma_commit_w(bar_v_empty((j + 1) % Cfg::NSV));
+      }
+      if (!ok) {
+        volatile int no_abort = 0;
+        const ptx::WaitCtx drain{&no_abort, nullptr, kWaitLimitNs};
+        ptx::mma_commit_w(bar_drain);
+        ptx::mbar_wait_w(bar_drain, 0, kSiteDrain, drain);
+      }
+    }
+  } else if (warp == 10) {
+    // ------------------------------------------------------------ MMA issuer of dQ (whole warp)
+    // A second issuing warp: dQ(j) waits only for dS(j), so its wait never
+    // holds back S and dP of the next key tile.  It reads TMEM columns of its
+    // own (the dS buffers) and writes the dQ accumulator, which no MMA of the
+    // other warp touches; K(j) was last read by S(j), complete before the
+    // compute warps could publish dS(j).
+    if (n_kv > 0) {
+      constexpr uint32_t idQ = ptx::idesc_bf16_f32(BT, DQK, false, true);  // dQ: B = K as MN-major
+      const uint32_t tDQ = tmem + Cfg::tDQ;
+      bool ok = true;
+      for (int j = 0; j < n_kv; ++j) {
         // dQ(j) += dS(j) K(j), dS(j) in buffer j % NB
         if (!ptx::mbar_wait_w(bar_ds_full, j & 1, kSiteDSFull, wctx)) { ok = false; break; }
         ptx::tc_fence_after();
-        const uint64_t kd = ptx::sdesc_sw128(kb(j), kPanel, 1024);
+        const uint64_t kd = ptx::sdesc_sw128(sbase + Cfg::offK + (j % Cfg::NSK) * Cfg::kKBytes, kPanel, 1024);
         const uint32_t tA = tmem + Cfg::tDS + 64 * (j % NB);
 #pragma unroll
         for (int kk = 0; kk < BT / 16; ++kk)
@@ -737,12 +759,13 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dq_kernel(const __grid_c
         ptx::mma_commit_w(bar_dq_done(j % NB));
         ptx::mma_commit_w(bar_k_empty(j % Cfg::NSK));
       }
-      if (ok) ptx::mma_commit_w(bar_final);
-      if (!ok) {
+      if (ok) {
+        ptx::mma_commit_w(bar_final);
+      } else {
         volatile int no_abort = 0;
         const ptx::WaitCtx drain{&no_abort, nullptr, kWaitLimitNs};
-        ptx::mma_commit_w(bar_drain);
-        ptx::mbar_wait_w(bar_drain, 0, kSiteDrain, drain);
+        ptx::mma_commit_w(bar_drain2);
+        ptx::mbar_wait_w(bar_drain2, 0, kSiteDrain, drain);
       }
     }
   } else {
@@ -868,7 +891,7 @@ cudaError_t launch_dq(const AttnArgs& a, cudaStream_t st) {
   if (e != cudaSuccess) return e;
   const int64_t grid = int64_t(a.num_tiles) * a.hq;
   if (grid == 0) return cudaSuccess;
-  attn_bwd_dq_kernel<DQK><<<unsigned(grid), kThreads, Cfg::kSmem, st>>>(p);
+  attn_bwd_dq_kernel<DQK><<<unsigned(grid), kThreadsDq, Cfg::kSmem, st>>>(p);
   return cudaGetLastError();
 }
 
