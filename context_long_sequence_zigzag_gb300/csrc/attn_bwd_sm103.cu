@@ -38,7 +38,8 @@
 // In both kernels two groups of four compute warps split the N columns
 // (group g owns the g-th half, thread = TMEM lane); each group writes its
 // bf16 result only into TMEM columns it has already read.  Roles: warps 0-7
-// compute, warp 8 TMA producer, warp 9 TMEM allocator + MMA issuer; the dQ
+// compute, warp 8 TMA producers (lanes 0 and 1, one stream each), warp 9
+// TMEM allocator + MMA issuer; the dQ
 // kernel adds warp 10, which issues the dQ MMAs so that waiting for dS never
 // delays S and dP of the next key tile.  MMA-issuing warps run converged and
 // elect one lane per instruction.
@@ -220,7 +221,7 @@ struct DkdvCfg {
   static constexpr uint32_t offO = offQ + NS * kQBytes;  // NS stages
   static constexpr uint32_t offStat = offO + NS * kOBytes;  // [2][2*BNQ] floats
   static constexpr uint32_t offBar = offStat + 2 * 2 * BNQ * 4;
-  static constexpr int kNumBars = 1 + 2 * NS + 9;
+  static constexpr int kNumBars = 1 + 3 * NS + 9;
   static constexpr uint32_t kSmem = offBar + kNumBars * 8 + 16;
   // TMEM columns
   static constexpr uint32_t tS = 0, tDP = BNQ, tDV = 2 * BNQ, tDK = 2 * BNQ + DV;
@@ -250,9 +251,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dkdv_kernel(const __grid
 
   const uint32_t bar0 = sbase + Cfg::offBar;
   const uint32_t bar_kv = bar0;
-  auto bar_q_full = [&](int s) { return bar0 + 8u * (1 + s); };
+  auto bar_q_full = [&](int s) { return bar0 + 8u * (1 + s); };                  // Q of stage s landed
   auto bar_q_empty = [&](int s) { return bar0 + 8u * (1 + Cfg::NS + s); };
-  const uint32_t bar_s_full = bar0 + 8u * (1 + 2 * Cfg::NS);
+  auto bar_o_full = [&](int s) { return bar0 + 8u * (1 + 2 * Cfg::NS + s); };   // dO of stage s landed
+  const uint32_t bar_s_full = bar0 + 8u * (1 + 3 * Cfg::NS);
   const uint32_t bar_dp_full = bar_s_full + 8;
   const uint32_t bar_p_full = bar_s_full + 16;
   const uint32_t bar_ds_full = bar_s_full + 24;
@@ -268,6 +270,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dkdv_kernel(const __grid
     for (int s = 0; s < Cfg::NS; ++s) {
       ptx::mbar_init(bar_q_full(s), 1);
       ptx::mbar_init(bar_q_empty(s), 1);
+      ptx::mbar_init(bar_o_full(s), 1);
     }
     ptx::mbar_init(bar_s_full, 1);
     ptx::mbar_init(bar_dp_full, 1);
@@ -297,35 +300,46 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dkdv_kernel(const __grid
   const ptx::WaitCtx wctx{abort_flag, p.err, kWaitLimitNs};
 
   if (warp == 8) {
-    // ------------------------------------------------------------ producer
-    if (lane == 0 && n_steps > 0) {
+    // ------------------------------------------------------------ producers
+    // Lane 0 loads the K/V tile, then streams Q; lane 1 streams dO.  On GB300
+    // one thread's tiled TMA loads top out near 40 B/cycle, two reach ~60.
+    if (lane < 2 && n_steps > 0) {
+      const bool qstream = lane == 0;
       int issued = 0;
-      ptx::mbar_arrive_expect_tx(bar_kv, Cfg::kKBytes + Cfg::kVBytes);
-      for (int c = 0; c < Cfg::kKPanels; ++c)
-        ptx::tma_load_3d(sbase + Cfg::offK + c * kPanel, &p.tk, bar_kv, c * 64, kvh, tile.row0);
-      for (int c = 0; c < 2; ++c)
-        ptx::tma_load_3d(sbase + Cfg::offV + c * kPanel, &p.tv, bar_kv, c * 64, kvh, tile.row0);
+      if (qstream) {
+        ptx::mbar_arrive_expect_tx(bar_kv, Cfg::kKBytes + Cfg::kVBytes);
+        for (int c = 0; c < Cfg::kKPanels; ++c)
+          ptx::tma_load_3d(sbase + Cfg::offK + c * kPanel, &p.tk, bar_kv, c * 64, kvh, tile.row0);
+        for (int c = 0; c < 2; ++c)
+          ptx::tma_load_3d(sbase + Cfg::offV + c * kPanel, &p.tv, bar_kv, c * 64, kvh, tile.row0);
+      }
+      auto full = [&](int st) { return qstream ? bar_q_full(st) : bar_o_full(st); };
       StepCursor<BNQ> cur;
       cur.init(a.ranges, tile.range_begin, tile.range_count, G, kvh, a.hkv, a.gqa_interleaved);
       for (int i = 0; i < n_steps; ++i, cur.next()) {
-        const int s = i % Cfg::NS;
-        if (i >= Cfg::NS && !ptx::mbar_wait(bar_q_empty(s), ((i / Cfg::NS) - 1) & 1, kSiteQEmpty, wctx)) break;
-        ptx::mbar_arrive_expect_tx(bar_q_full(s), Cfg::kQBytes + Cfg::kOBytes);
+        const int st = i % Cfg::NS;
+        // stage st is free once dK of its previous occupant (the last reader of Q and dO) completed
+        if (i >= Cfg::NS && !ptx::mbar_wait(bar_q_empty(st), ((i / Cfg::NS) - 1) & 1, kSiteQEmpty, wctx)) break;
         const int h = cur.head();
-        for (int c = 0; c < Cfg::kKPanels; ++c)
-          ptx::tma_load_3d(sbase + Cfg::offQ + s * Cfg::kQBytes + c * Cfg::kQPanel, &p.tq, bar_q_full(s), c * 64, h,
-                           cur.row());
-        for (int c = 0; c < 2; ++c)
-          ptx::tma_load_3d(sbase + Cfg::offO + s * Cfg::kOBytes + c * Cfg::kQPanel, &p.tdo, bar_q_full(s), c * 64,
-                           h, cur.row());
+        if (qstream) {
+          ptx::mbar_arrive_expect_tx(full(st), Cfg::kQBytes);
+          for (int c = 0; c < Cfg::kKPanels; ++c)
+            ptx::tma_load_3d(sbase + Cfg::offQ + st * Cfg::kQBytes + c * Cfg::kQPanel, &p.tq, full(st), c * 64, h,
+                             cur.row());
+        } else {
+          ptx::mbar_arrive_expect_tx(full(st), Cfg::kOBytes);
+          for (int c = 0; c < 2; ++c)
+            ptx::tma_load_3d(sbase + Cfg::offO + st * Cfg::kOBytes + c * Cfg::kQPanel, &p.tdo, full(st), c * 64, h,
+                             cur.row());
+        }
         ++issued;
       }
       if (*abort_flag) {
         volatile int no_abort = 0;
         const ptx::WaitCtx drain{&no_abort, nullptr, kWaitLimitNs};
-        ptx::mbar_wait(bar_kv, 0, kSiteDrain, drain);
+        if (qstream) ptx::mbar_wait(bar_kv, 0, kSiteDrain, drain);
         for (int i = max(0, issued - Cfg::NS); i < issued; ++i)
-          ptx::mbar_wait(bar_q_full(i % Cfg::NS), (i / Cfg::NS) & 1, kSiteDrain, drain);
+          ptx::mbar_wait(full(i % Cfg::NS), (i / Cfg::NS) & 1, kSiteDrain, drain);
       }
     }
   } else if (warp == 9) {
@@ -369,6 +383,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dkdv_kernel(const __grid
           issue_ts(tDK, tDP, qb(i - 1), idDK, i - 1 > 0);
           ptx::mma_commit_w(bar_q_empty((i - 1) % Cfg::NS));
         }
+        if (!ptx::mbar_wait_w(bar_o_full(i % Cfg::NS), (i / Cfg::NS) & 1, kSiteQFull, wctx)) { ok = false; break; }
+        ptx::tc_fence_after();
         issue_ss(tDP, vb, ob(i), DV / 16);
         ptx::mma_commit_w(bar_dp_full);
         // dV(i) needs P(i); once it is issued, S(i+1) may overwrite tS
@@ -548,24 +564,28 @@ struct KvCursor {
 
 template <int DQK>
 struct DqCfg {
-  // K(j) is read by S(j) and, one step later in issue order, by dQ(j); V(j)
-  // only by dP(j): K gets the deeper ring.
+  // 128-wide heads keep Q in TMEM (64 packed columns after the single dS
+  // buffer), so S = Q K^T is a TS MMA and Q's shared memory goes to a
+  // fourth K stage.  K(j) is read by S(j) and, later, by dQ(j); V(j) only
+  // by dP(j): K gets the deeper ring.
+  static constexpr bool kQTmem = DQK == 128;
   static constexpr int kKPanels = DQK / 64;
-  static constexpr int NSK = DQK == 128 ? 3 : 2;
+  static constexpr int NSK = DQK == 128 ? 4 : 2;
   static constexpr int NSV = DQK == 128 ? 2 : 1;
-  static constexpr int NB = DQK == 128 ? 2 : 1;  // dS buffers
+  static constexpr int NB = 1;  // dS buffers
   static constexpr uint32_t kKBytes = kKPanels * kPanel;
   static constexpr uint32_t kVBytes = 2 * kPanel;
+  static constexpr uint32_t kQBytes = kQTmem ? 0 : kKBytes;  // Q panels in shared memory
   static constexpr uint32_t offQ = 0;
-  static constexpr uint32_t offO = offQ + kKBytes;
+  static constexpr uint32_t offO = offQ + kQBytes;
   static constexpr uint32_t offK = offO + kVBytes;           // NSK stages
   static constexpr uint32_t offV = offK + NSK * kKBytes;     // NSV stages
   static constexpr uint32_t offBar = offV + NSV * kVBytes;
-  static constexpr int kNumBars = 1 + 2 * NSK + 2 * NSV + 8 + NB;
+  static constexpr int kNumBars = 1 + 2 * NSK + 2 * NSV + 9 + NB;
   static constexpr uint32_t kSmem = offBar + kNumBars * 8 + 16;
   // TMEM columns
-  static constexpr uint32_t tS = 0, tDP = 128, tDQ = 256, tDS = 256 + DQK;
-  static_assert(tDS + 64 * NB <= 512, "TMEM budget");
+  static constexpr uint32_t tS = 0, tDP = 128, tDQ = 256, tDS = 256 + DQK, tQ = tDS + 64 * NB;
+  static_assert(tQ + (kQTmem ? DQK / 2 : 0) <= 512, "TMEM budget");
   static_assert(kSmem <= 232448, "shared memory budget");
 };
 
@@ -602,6 +622,7 @@ __global__ void __launch_bounds__(kThreadsDq, 1) attn_bwd_dq_kernel(const __grid
   const uint32_t bar_dp_read = bar_s_full + 48;                        // compute warps hold dP(j)
   auto bar_dq_done = [&](int b) { return bar_s_full + 56 + 8u * b; };  // dQ(j) read dS buffer b = j % NB
   const uint32_t bar_drain2 = bar_s_full + 56 + 8u * NB;            // drain of the dQ issuer
+  const uint32_t bar_qt = bar_s_full + 64 + 8u * NB;                // Q rows written into TMEM (8 warps)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Cfg::offBar + Cfg::kNumBars * 8);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Cfg::offBar + Cfg::kNumBars * 8 + 4);
 
@@ -624,6 +645,7 @@ __global__ void __launch_bounds__(kThreadsDq, 1) attn_bwd_dq_kernel(const __grid
     ptx::mbar_init(bar_dp_read, 8);
     for (int b = 0; b < NB; ++b) ptx::mbar_init(bar_dq_done(b), 1);
     ptx::mbar_init(bar_drain2, 1);
+    ptx::mbar_init(bar_qt, 8);
     *abort_flag = 0;
     ptx::fence_barrier_init();
   }
@@ -644,39 +666,42 @@ __global__ void __launch_bounds__(kThreadsDq, 1) attn_bwd_dq_kernel(const __grid
   const ptx::WaitCtx wctx{abort_flag, p.err, kWaitLimitNs};
 
   if (warp == 8) {
-    // ------------------------------------------------------------ producer
-    if (lane == 0 && n_kv > 0) {
-      int issued = 0, issued_v = 0;
-      ptx::mbar_arrive_expect_tx(bar_q, Cfg::kKBytes + Cfg::kVBytes);
-      for (int c = 0; c < Cfg::kKPanels; ++c)
-        ptx::tma_load_3d(sbase + Cfg::offQ + c * kPanel, &p.tq, bar_q, c * 64, h, tile.row0);
-      for (int c = 0; c < 2; ++c)
-        ptx::tma_load_3d(sbase + Cfg::offO + c * kPanel, &p.tdo, bar_q, c * 64, h, tile.row0);
+    // ------------------------------------------------------------ producers
+    // Lane 0 streams K; lane 1 loads Q / dO, then streams V.  On GB300 one
+    // thread's tiled TMA loads top out near 40 B/cycle, two reach about 60.
+    if (lane < 2 && n_kv > 0) {
+      const bool kstream = lane == 0;
+      const int NS = kstream ? Cfg::NSK : Cfg::NSV;
+      const uint32_t bytes = kstream ? Cfg::kKBytes : Cfg::kVBytes;
+      const int panels = kstream ? Cfg::kKPanels : 2;
+      const uint32_t base = sbase + (kstream ? Cfg::offK : Cfg::offV);
+      const CUtensorMap* map = kstream ? &p.tk : &p.tv;
+      auto full = [&](int st) { return kstream ? bar_k_full(st) : bar_v_full(st); };
+      auto empty = [&](int st) { return kstream ? bar_k_empty(st) : bar_v_empty(st); };
+      if (!kstream) {
+        ptx::mbar_arrive_expect_tx(bar_q, Cfg::kQBytes + Cfg::kVBytes);
+        if (!Cfg::kQTmem)
+          for (int c = 0; c < Cfg::kKPanels; ++c)
+            ptx::tma_load_3d(sbase + Cfg::offQ + c * kPanel, &p.tq, bar_q, c * 64, h, tile.row0);
+        for (int c = 0; c < 2; ++c)
+          ptx::tma_load_3d(sbase + Cfg::offO + c * kPanel, &p.tdo, bar_q, c * 64, h, tile.row0);
+      }
+      int issued = 0;
       KvCursor cur;
       cur.init(a.ranges, tile.range_begin, tile.range_count);
       for (int j = 0; j < n_kv; ++j, cur.next()) {
-        const int sk = j % Cfg::NSK, sv = j % Cfg::NSV;
-        if (j >= Cfg::NSK && !ptx::mbar_wait(bar_k_empty(sk), ((j / Cfg::NSK) - 1) & 1, kSiteKVEmpty, wctx)) break;
-        ptx::mbar_arrive_expect_tx(bar_k_full(sk), Cfg::kKBytes);
-        for (int c = 0; c < Cfg::kKPanels; ++c)
-          ptx::tma_load_3d(sbase + Cfg::offK + sk * Cfg::kKBytes + c * kPanel, &p.tk, bar_k_full(sk), c * 64, kvh,
-                           cur.row());
+        const int st = j % NS;
+        if (j >= NS && !ptx::mbar_wait(empty(st), ((j / NS) - 1) & 1, kSiteKVEmpty, wctx)) break;
+        ptx::mbar_arrive_expect_tx(full(st), bytes);
+        for (int c = 0; c < panels; ++c)
+          ptx::tma_load_3d(base + st * bytes + c * kPanel, map, full(st), c * 64, kvh, cur.row());
         ++issued;
-        if (j >= Cfg::NSV && !ptx::mbar_wait(bar_v_empty(sv), ((j / Cfg::NSV) - 1) & 1, kSiteKVEmpty, wctx)) break;
-        ptx::mbar_arrive_expect_tx(bar_v_full(sv), Cfg::kVBytes);
-        for (int c = 0; c < 2; ++c)
-          ptx::tma_load_3d(sbase + Cfg::offV + sv * Cfg::kVBytes + c * kPanel, &p.tv, bar_v_full(sv), c * 64, kvh,
-                           cur.row());
-        ++issued_v;
       }
       if (*abort_flag) {
         volatile int no_abort = 0;
         const ptx::WaitCtx drain{&no_abort, nullptr, kWaitLimitNs};
-        ptx::mbar_wait(bar_q, 0, kSiteDrain, drain);
-        for (int j = max(0, issued - Cfg::NSK); j < issued; ++j)
-          ptx::mbar_wait(bar_k_full(j % Cfg::NSK), (j / Cfg::NSK) & 1, kSiteDrain, drain);
-        for (int j = max(0, issued_v - Cfg::NSV); j < issued_v; ++j)
-          ptx::mbar_wait(bar_v_full(j % Cfg::NSV), (j / Cfg::NSV) & 1, kSiteDrain, drain);
+        if (!kstream) ptx::mbar_wait(bar_q, 0, kSiteDrain, drain);
+        for (int j = max(0, issued - NS); j < issued; ++j) ptx::mbar_wait(full(j % NS), (j / NS) & 1, kSiteDrain, drain);
       }
     }
   } else if (warp == 9) {
@@ -695,12 +720,25 @@ __global__ void __launch_bounds__(kThreadsDq, 1) attn_bwd_dq_kernel(const __grid
           ptx::mma_ss_w(d, da + off, db + off, idS, kk > 0);
         }
       };
-      bool ok = ptx::mbar_wait_w(bar_q, 0, kSiteQ, wctx) && ptx::mbar_wait_w(bar_k_full(0), 0, kSiteKVFull, wctx);
+      // S(j) = Q K(j)^T: TS with Q from TMEM (128-wide heads), else SS
+      auto issue_s = [&](int j) {
+        if constexpr (Cfg::kQTmem) {
+          const uint64_t kd = ptx::sdesc_sw128(kb(j), 16, 1024);
+#pragma unroll
+          for (int kk = 0; kk < DQK / 16; ++kk)
+            ptx::mma_ts_w(tS, tmem + Cfg::tQ + kk * 8, kd + (((kk >> 2) * kPanel + (kk & 3) * 32) >> 4), idS, kk > 0);
+        } else {
+          issue_ss(tS, qb, kb(j), DQK / 16);
+        }
+      };
+      bool ok = ptx::mbar_wait_w(Cfg::kQTmem ? bar_qt : bar_q, 0, kSiteQ, wctx) &&
+                ptx::mbar_wait_w(bar_k_full(0), 0, kSiteKVFull, wctx);
       if (ok) {
         ptx::tc_fence_after();
-        issue_ss(tS, qb, kb(0), DQK / 16);
+        issue_s(0);
         ptx::mma_commit_w(bar_s_full);
-        ok = ptx::mbar_wait_w(bar_v_full(0), 0, kSiteKVFull, wctx);
+        ok = (!Cfg::kQTmem || ptx::mbar_wait_w(bar_q, 0, kSiteQ, wctx)) &&
+             ptx::mbar_wait_w(bar_v_full(0), 0, kSiteKVFull, wctx);
       }
       if (ok) {
         ptx::tc_fence_after();
@@ -716,7 +754,7 @@ __global__ void __launch_bounds__(kThreadsDq, 1) attn_bwd_dq_kernel(const __grid
           break;
         }
         ptx::tc_fence_after();
-        issue_ss(tS, qb, kb(j + 1), DQK / 16);
+        issue_s(j + 1);
         ptx::mma_commit_w(bar_s_full);
         // dP(j+1) as soon as they have read dP(j)
         if (!ptx::mbar_wait_w(bar_dp_read, j & 1, kSiteDPFull, wctx) ||
@@ -781,6 +819,28 @@ __global__ void __launch_bounds__(kThreadsDq, 1) attn_bwd_dq_kernel(const __grid
     const int64_t qrow = int64_t(tile.row0) + r;
     const float lse2 = row_ok ? a.lse_in[int64_t(h) * a.T + qrow] * kLog2e : 0.f;
     const float dsc = row_ok ? a.dpsum[int64_t(h) * a.T + qrow] * a.scale : 0.f;
+    if (Cfg::kQTmem && n_kv > 0) {
+      // Q row -> TMEM, group g the g-th half (bf16 pairs are the A-operand
+      // packing).  Rows past the tile read the following rows (or zeros past
+      // the end); they are masked out of P.
+      const uint4* src = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(a.q) +
+                                                        (qrow * a.hq + h) * DQK) + grp * 8;
+      const bool in_range = qrow < a.T;
+      uint32_t qr[32];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const uint4 v = in_range ? __ldg(src + i) : make_uint4(0, 0, 0, 0);
+        qr[4 * i] = v.x;
+        qr[4 * i + 1] = v.y;
+        qr[4 * i + 2] = v.z;
+        qr[4 * i + 3] = v.w;
+      }
+      ptx::tmem_st32(tmem + lane_base + Cfg::tQ + grp * 32, qr);
+      ptx::tmem_st_wait();
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(bar_qt);
+    }
     bool ok = true;
     KvCursor cur;
     cur.init(a.ranges, tile.range_begin, tile.range_count);

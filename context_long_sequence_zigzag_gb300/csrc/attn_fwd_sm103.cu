@@ -27,7 +27,8 @@
 //              row maximum, exponentiates, writes P back to TMEM, rescales O
 //              when the reference maximum moves by more than 2^8, and finally
 //              normalises O and writes o / lse.
-//   warp 4     TMA producer: K and V tiles into three-deep rings.
+//   warp 4     TMA producers: lane 0 streams K, lane 1 streams V, each into
+//              its own ring.
 //   warp 5     TMEM allocator and MMA issuer.
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -176,34 +177,34 @@ __global__ void __launch_bounds__(192, 1) attn_fwd_tc_kernel(const __grid_consta
   const ptx::WaitCtx wctx{abort_flag, p.err, kWaitLimitNs};
 
   if (warp == 4) {
-    // ------------------------------------------------------------ producer
-    if (lane == 0 && n_kv > 0) {
-      int issued_k = 0, issued_v = 0;
+    // ------------------------------------------------------------ producers
+    // Lane 0 streams K, lane 1 streams V: on GB300 one thread's tiled TMA
+    // loads top out near 40 B/cycle, two issuing threads reach about 60.
+    if (lane < 2 && n_kv > 0) {
+      const bool kstream = lane == 0;
+      const int NS = kstream ? Cfg::NSK : Cfg::NSV;
+      const uint32_t bytes = kstream ? Cfg::kKBytes : Cfg::kVBytes;
+      const int panels = kstream ? Cfg::kQPanels : Cfg::kVPanels;
+      const uint32_t base = sbase + (kstream ? Cfg::offK : Cfg::offV);
+      const CUtensorMap* map = kstream ? &p.tk : &p.tv;
+      auto full = [&](int st) { return kstream ? bar_k_full(st) : bar_v_full(st); };
+      auto empty = [&](int st) { return kstream ? bar_k_empty(st) : bar_v_empty(st); };
+      int issued = 0;
       KvCursor cur;
       cur.init(a.ranges, tile.range_begin, tile.range_count);
       for (int j = 0; j < n_kv; ++j, cur.next()) {
-        const int sk = j % Cfg::NSK, sv = j % Cfg::NSV;
-        if (j >= Cfg::NSK && !ptx::mbar_wait(bar_k_empty(sk), ((j / Cfg::NSK) - 1) & 1, kSiteKEmpty, wctx)) break;
-        ptx::mbar_arrive_expect_tx(bar_k_full(sk), Cfg::kKBytes);
-        for (int c = 0; c < Cfg::kQPanels; ++c)
-          ptx::tma_load_3d(sbase + Cfg::offK + sk * Cfg::kKBytes + c * kSubTile, &p.tk, bar_k_full(sk), c * 64,
-                           kvh, cur.row());
-        ++issued_k;
-        if (j >= Cfg::NSV && !ptx::mbar_wait(bar_v_empty(sv), ((j / Cfg::NSV) - 1) & 1, kSiteVEmpty, wctx)) break;
-        ptx::mbar_arrive_expect_tx(bar_v_full(sv), Cfg::kVBytes);
-        for (int c = 0; c < Cfg::kVPanels; ++c)
-          ptx::tma_load_3d(sbase + Cfg::offV + sv * Cfg::kVBytes + c * kSubTile, &p.tv, bar_v_full(sv), c * 64,
-                           kvh, cur.row());
-        ++issued_v;
+        const int st = j % NS;
+        if (j >= NS && !ptx::mbar_wait(empty(st), ((j / NS) - 1) & 1, kstream ? kSiteKEmpty : kSiteVEmpty, wctx)) break;
+        ptx::mbar_arrive_expect_tx(full(st), bytes);
+        for (int c = 0; c < panels; ++c)
+          ptx::tma_load_3d(base + st * bytes + c * kSubTile, map, full(st), c * 64, kvh, cur.row());
+        ++issued;
       }
       if (*abort_flag) {
         // Let every copy still in flight land before the CTA exits.
         volatile int no_abort = 0;
         const ptx::WaitCtx drain{&no_abort, nullptr, kWaitLimitNs};
-        for (int j = max(0, issued_k - Cfg::NSK); j < issued_k; ++j)
-          ptx::mbar_wait(bar_k_full(j % Cfg::NSK), (j / Cfg::NSK) & 1, kSiteDrain, drain);
-        for (int j = max(0, issued_v - Cfg::NSV); j < issued_v; ++j)
-          ptx::mbar_wait(bar_v_full(j % Cfg::NSV), (j / Cfg::NSV) & 1, kSiteDrain, drain);
+        for (int j = max(0, issued - NS); j < issued; ++j) ptx::mbar_wait(full(j % NS), (j / NS) & 1, kSiteDrain, drain);
       }
     }
   } else if (warp == 5) {
