@@ -79,12 +79,23 @@ def oracle_sample(w: workloads.Workload, budget_tokens: int = 8192):
     return flops / dt / 1e12, dt, desc
 
 
+def kernel_source_digest(src: str) -> str:
+    """First 16 hex digits of the sha256 over a kernel's .cu file followed by
+    the two headers every kernel includes (internal.h, sm103_ptx.cuh)."""
+    import hashlib
+
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "context_long_sequence_zigzag_gb300", "csrc")
+    for name in (src, "internal.h", "sm103_ptx.cuh"):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
 def recorded_traffic(kernel: str, workload: str):
     """DRAM bytes per launch of `kernel` from the committed ncu summary
     (profiles/dram_traffic.txt), or None when none was recorded for this
     kernel and workload or the kernel's source changed since the capture."""
-    import hashlib
-
     path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
     if not os.path.exists(path):
         return None
@@ -92,8 +103,7 @@ def recorded_traffic(kernel: str, workload: str):
            "attn_bwd_dq_kernel": "attn_bwd_sm103.cu"}.get(kernel)
     if src is None:
         return None
-    with open(os.path.join(ROOT, "context_long_sequence_zigzag_gb300", "csrc", src), "rb") as f:
-        digest = hashlib.sha256(f.read()).hexdigest()[:16]
+    digest = kernel_source_digest(src)
     with open(path) as f:
         for line in f:
             fields = dict(tok.split("=", 1) for tok in line.split() if "=" in tok)
