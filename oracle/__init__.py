@@ -16,8 +16,8 @@ Contents and the passage each follows:
   earlier blocks are fully visible); "LLM context parallel production guide"
   sections "核心原理" (the result is exact attention) and "变长序列" (packed
   sequences never attend across their boundaries).
-* ``sharding``   — the global <-> sharded token order for contiguous and zigzag
-  placement.  "Ulysses与Ring-Attention详解" §4.2 (zigzag pairs block i with
+* ``sharding``   — the global <-> sharded token order for contiguous, zigzag and
+  striped placement, and the per-rank visible-pair counts.  "Ulysses与Ring-Attention详解" §4.2 (zigzag pairs block i with
   block 2C-1-i); "超长上下文训练速度翻倍秘籍" §3 varlen CP (every sub-sequence
   is itself cut into CP pieces).
 * ``merge``      — the exact log-sum-exp merge of two partial results.
@@ -42,6 +42,8 @@ from .sharding import (  # noqa: F401
     rank_chunks,
     shard_order,
     rank_offsets,
+    rank_visible_pairs,
+    striped_rows,
     to_sharded,
     to_global,
 )

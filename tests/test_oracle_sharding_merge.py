@@ -97,6 +97,69 @@ def test_zigzag_balances_causal_work_and_contiguous_does_not():
     assert sum(z) == sum(c) == (64 * 16) * (64 * 16 + 1) // 2
 
 
+def test_striped_worked_example():
+    # "LLM context parallel production guide", 因果 Attention 会制造 Rank 负载不均
+    # (striped token placement): token t of each sequence goes to rank t mod C.
+    # Written out by hand for two packed sequences of 10 and 3 tokens, C = 4.
+    cu = [0, 10, 13]
+    want = [0, 4, 8, 10,  # rank 0: tokens 0, 4, 8 of seq 0; token 0 of seq 1
+            1, 5, 9, 11,  # rank 1
+            2, 6, 12,     # rank 2
+            3, 7]         # rank 3: seq 1 has no token 3
+    assert oracle.shard_order(cu, 4, "striped").tolist() == want
+    assert oracle.rank_offsets(cu, 4, "striped").tolist() == [0, 4, 8, 11, 13]
+
+
+@pytest.mark.parametrize("C", [1, 2, 3, 8])
+def test_striped_varlen_permutation(C):
+    lengths = [1, 2, 7, 64, 65, 300, 5]
+    cu = workloads.make_cu_seqlens(lengths).tolist()
+    T = cu[-1]
+    perm = oracle.shard_order(cu, C, "striped")
+    assert sorted(perm.tolist()) == list(range(T))
+    off = oracle.rank_offsets(cu, C, "striped")
+    seq_of = np.searchsorted(np.asarray(cu), np.arange(T), side="right") - 1
+    pos = np.arange(T) - np.asarray(cu)[seq_of]
+    for r in range(C):
+        part = perm[off[r]:off[r + 1]]
+        # exactly the tokens at positions = r (mod C), sequences in order,
+        # positions increasing by C inside a sequence
+        assert set(part.tolist()) == set(np.nonzero(pos % C == r)[0].tolist())
+        assert np.all(np.diff(seq_of[part]) >= 0)
+        for s in range(len(lengths)):
+            ps = pos[part[seq_of[part] == s]]
+            assert np.all(np.diff(ps) == C)
+
+
+def test_rank_visible_pairs_closed_forms():
+    # one sequence of L = C*m tokens: causal query t sees t + 1 keys
+    C, m = 8, 16
+    L = C * m
+    striped = oracle.rank_visible_pairs([0, L], C, "striped")
+    contig = oracle.rank_visible_pairs([0, L], C, "contiguous")
+    zig = oracle.rank_visible_pairs([0, L], C, "zigzag")
+    for r in range(C):
+        # striped rank r holds t = r + C*k, k < m: sum (t + 1)
+        assert striped[r] == m * (r + 1) + C * m * (m - 1) // 2
+        # contiguous rank r holds t in [r*m, (r+1)*m)
+        assert contig[r] == m * r * m + m * (m + 1) // 2
+    assert len(set(zig.tolist())) == 1
+    assert striped.sum() == contig.sum() == zig.sum() == L * (L + 1) // 2
+    # striped is nearly balanced, contiguous is not
+    assert striped.max() / striped.min() < 1 + 2.0 / m
+    assert contig.max() / contig.min() > C
+    # non-causal: every query sees its whole sequence
+    cu = [0, 10, 13]
+    nc = oracle.rank_visible_pairs(cu, 4, "striped", causal=False)
+    assert nc.tolist() == [3 * 10 + 3, 3 * 10 + 3, 2 * 10 + 3, 2 * 10]
+
+
+def test_rank_visible_pairs_agrees_with_direct_count():
+    cu = workloads.make_cu_seqlens([33, 1, 90]).tolist()
+    for layout in ("contiguous", "zigzag", "striped"):
+        assert oracle.rank_visible_pairs(cu, 4, layout).tolist() == _rank_visible_pairs(cu, 4, layout)
+
+
 # ---------------------------------------------------------------- merge
 
 def test_merge_identity_and_equal_halves():
@@ -149,7 +212,7 @@ def test_merge_over_any_key_partition_equals_full_attention():
         np.testing.assert_allclose(l_acc, l_full, atol=1e-13)
 
 
-@pytest.mark.parametrize("layout", ["contiguous", "zigzag"])
+@pytest.mark.parametrize("layout", ["contiguous", "zigzag", "striped"])
 def test_ring_of_shards_equals_full_attention(layout):
     # Each virtual rank merges its (q shard, kv shard) blocks in ring order
     # r, r-1, ... mod C; the result un-permuted is unsharded attention.
