@@ -320,6 +320,8 @@ def run_gpu(args):
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     w = workloads.get(args.workload)
+    if args.layout:
+        w = w.replace(layout=args.layout)
     r = Runner(w, dev)
     cpa = r.cpa
 
@@ -417,6 +419,7 @@ def run_gpu(args):
             "clocks": clk,
             "gpu_launches": r.launches_per_step * args.steps,
             "rank_block_counts": cpa.cp_rank_block_counts(r.prob),
+            "rank_balance": balance_report(cpa, w),
         }
         if not args.no_cpu_baseline:
             tf, secs, desc = oracle_sample(w, args.cpu_tokens)
@@ -425,6 +428,20 @@ def run_gpu(args):
     if world > 1:
         torch.distributed.destroy_process_group()
     return result
+
+
+def balance_report(cpa, w) -> dict:
+    """Per-rank effective attention work of the workload under each shard
+    layout: visible 128x128 tiles per rank (cp_rank_block_counts) and the
+    slowest rank's share over the mean.  With one GPU per rank, the slowest
+    rank would set the step time."""
+    out = {}
+    cu = workloads.make_cu_seqlens(w.lengths()).tolist()
+    for layout in ("contiguous", "zigzag", "striped"):
+        p = cpa.Problem(w.total_tokens, w.hq, w.hkv, w.d_qk, w.d_v, w.cp_size, layout, cu, w.causal, w.scale)
+        c = cpa.cp_rank_block_counts(p)
+        out[layout] = {"max_over_mean": round(max(c) / (sum(c) / len(c)), 4), "min": min(c), "max": max(c)}
+    return out
 
 
 def run_reference(args):
@@ -464,6 +481,8 @@ def main():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=list(workloads.WORKLOADS))
     ap.add_argument("--cpu-tokens", type=int, default=8192)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--layout", default=None, choices=["contiguous", "zigzag", "striped"],
+                    help="shard layout instead of the workload's own (zigzag for the standard ones)")
     args = ap.parse_args()
     if args.impl == "reference":
         res = run_reference(args)

@@ -1,7 +1,7 @@
 """context_long_sequence_zigzag_gb300 — Python binding of libcpattn.
 
 Context-parallel exact causal attention on one GB300: a (packed) sequence is
-cut into C context-parallel shards, contiguous or zigzag; the C virtual ranks
+cut into C context-parallel shards (contiguous, zigzag or striped); the C virtual ranks
 share one GPU and the KV ring is the order in which the kernels visit the
 HBM-resident KV shards.  The C ABI (``include/cp_attn.h``) is the product;
 this module only marshals torch tensors into its pointers and sizes.  Every
@@ -35,7 +35,7 @@ if not os.path.exists(LIB_PATH):
 _lib = ctypes.CDLL(LIB_PATH)
 
 CP_OK, CP_ERR_INVALID_ARG, CP_ERR_UNSUPPORTED, CP_ERR_CUDA, CP_ERR_DEVICE_TIMEOUT, CP_ERR_WORKSPACE = range(6)
-CP_LAYOUT_CONTIGUOUS, CP_LAYOUT_ZIGZAG = 0, 1
+CP_LAYOUT_CONTIGUOUS, CP_LAYOUT_ZIGZAG, CP_LAYOUT_STRIPED = 0, 1, 2
 CP_DT_F32, CP_DT_BF16 = 0, 1
 CP_GQA_BLOCKED, CP_GQA_INTERLEAVED = 0, 1
 CP_OP_FWD, CP_OP_BWD, CP_OP_BLOCK_FWD, CP_OP_PERMUTE, CP_OP_BWD_DKDV, CP_OP_BWD_DQ = 0, 1, 2, 3, 4, 5
@@ -129,7 +129,8 @@ class Problem:
             total_tokens=int(total_tokens), num_seqs=len(cu) - 1, hq=hq, hkv=hkv,
             cu_seqlens=ctypes.cast(self._cu_arr, ctypes.POINTER(ctypes.c_int32)),
             d_qk=d_qk, d_v=d_v, cp_size=cp_size,
-            layout={"contiguous": CP_LAYOUT_CONTIGUOUS, "zigzag": CP_LAYOUT_ZIGZAG}[layout],
+            layout={"contiguous": CP_LAYOUT_CONTIGUOUS, "zigzag": CP_LAYOUT_ZIGZAG,
+                    "striped": CP_LAYOUT_STRIPED}[layout],
             causal=int(bool(causal)),
             scale=float(scale if scale is not None else 1.0 / math.sqrt(d_qk)),
             gqa={"blocked": CP_GQA_BLOCKED, "interleaved": CP_GQA_INTERLEAVED}[gqa],

@@ -20,19 +20,38 @@
 namespace cpattn {
 namespace {
 
+// One rank's run of one sequence, stored contiguously in sharded order.  Its
+// tokens sit at global rows grow0, grow0 + stride, ... (stride 1 except for
+// the striped layout, where it is C).
 struct Chunk {
   int32_t seq, idx, pos0, len, rank;
-  int64_t grow0;  // first global row
-  int64_t srow0;  // first sharded row
+  int64_t grow0;   // first global row
+  int64_t srow0;   // first sharded row
+  int32_t stride;  // global-row step between consecutive tokens of the chunk
 };
 
 struct ShardMap {
   int32_t C = 0, S = 0, per = 0;  // ranks, sequences, chunks per rank per sequence
+  bool striped = false;
   std::vector<Chunk> chunks;      // index (r * S + s) * per + k
   std::vector<int64_t> rank_off;  // C + 1
 
   const Chunk& at(int r, int s, int k) const { return chunks[(size_t(r) * S + s) * per + k]; }
 };
+
+// Position of chunk X's first token in the coordinates of a (query chunk A,
+// key chunk B) block.  Contiguous and zigzag chunks hold consecutive
+// positions, so that is X.pos0.  A striped chunk of rank r holds positions
+// r, r + C, r + 2C, ...: key j of rank rk is visible to query i of rank rq
+// iff rk + C*j <= rq + C*i, i.e. iff j + [rk > rq] <= i.  Queries therefore
+// take their index inside the chunk as position and keys of a higher rank
+// are shifted by one; positions stay consecutive inside every chunk.
+int32_t key_pos0(const ShardMap& m, const Chunk& key, const Chunk& query) {
+  return m.striped ? (key.rank > query.rank ? 1 : 0) : key.pos0;
+}
+int32_t query_pos0(const ShardMap& m, const Chunk& query, const Chunk& key) {
+  return m.striped ? (key.rank > query.rank ? -1 : 0) : query.pos0;
+}
 
 std::vector<int32_t> seqlens_of(const cp_desc_t* d) {
   std::vector<int32_t> cu;
@@ -50,7 +69,8 @@ cp_status_t check_map_fields(const cp_desc_t* d) {
   if (d->total_tokens < 0 || d->total_tokens > INT32_MAX) return CP_ERR_INVALID_ARG;
   if (d->num_seqs < 1) return CP_ERR_INVALID_ARG;
   if (d->cp_size < 1 || d->cp_size > 4096) return CP_ERR_INVALID_ARG;
-  if (d->layout != CP_LAYOUT_CONTIGUOUS && d->layout != CP_LAYOUT_ZIGZAG) return CP_ERR_INVALID_ARG;
+  if (d->layout != CP_LAYOUT_CONTIGUOUS && d->layout != CP_LAYOUT_ZIGZAG && d->layout != CP_LAYOUT_STRIPED)
+    return CP_ERR_INVALID_ARG;
   if (d->cu_seqlens == nullptr) {
     if (d->num_seqs != 1) return CP_ERR_INVALID_ARG;
     return CP_OK;
@@ -87,6 +107,7 @@ ShardMap build_map(const cp_desc_t* d) {
   m.C = d->cp_size;
   m.S = int32_t(cu.size()) - 1;
   m.per = d->layout == CP_LAYOUT_ZIGZAG ? 2 : 1;
+  m.striped = d->layout == CP_LAYOUT_STRIPED;
   const int64_t n = int64_t(m.C) * m.per;  // pieces per sequence
   m.chunks.reserve(size_t(m.C) * m.S * m.per);
   m.rank_off.assign(m.C + 1, 0);
@@ -95,6 +116,20 @@ ShardMap build_map(const cp_desc_t* d) {
     m.rank_off[r] = srow;
     for (int s = 0; s < m.S; ++s) {
       const int64_t L = int64_t(cu[s + 1]) - cu[s];
+      if (m.striped) {
+        Chunk ch;
+        ch.seq = s;
+        ch.idx = r;
+        ch.pos0 = 0;  // block-relative positions: see key_pos0 / query_pos0
+        ch.len = int32_t(L > r ? (L - r + m.C - 1) / m.C : 0);
+        ch.rank = r;
+        ch.grow0 = cu[s] + r;
+        ch.srow0 = srow;
+        ch.stride = m.C;
+        m.chunks.push_back(ch);
+        srow += ch.len;
+        continue;
+      }
       for (int k = 0; k < m.per; ++k) {
         const int64_t c = (k == 0) ? r : (2 * int64_t(m.C) - 1 - r);
         const int64_t lo = (c * L) / n, hi = ((c + 1) * L) / n;
@@ -106,6 +141,7 @@ ShardMap build_map(const cp_desc_t* d) {
         ch.rank = r;
         ch.grow0 = cu[s] + lo;
         ch.srow0 = srow;
+        ch.stride = 1;
         m.chunks.push_back(ch);
         srow += hi - lo;
       }
@@ -148,12 +184,13 @@ Plan build_fwd_plan(const cp_desc_t* d, const ShardMap& m, int q_rank, int kv_ra
           const Chunk& B = m.at(rho, A.seq, k);
           if (B.len == 0) continue;
           RangeDesc r{};
+          const int32_t bpos = key_pos0(m, B, A);
           r.row0 = int32_t(B.srow0);
-          r.pos0 = B.pos0;
+          r.pos0 = bpos;
           if (causal) {
-            if (B.pos0 > qmax) continue;  // entirely in the future: skipped
-            r.nrows = std::min(B.len, qmax - B.pos0 + 1);
-            r.flags = (B.pos0 + r.nrows - 1 > qmin) ? kRangeMasked : 0;
+            if (bpos > qmax) continue;  // entirely in the future: skipped
+            r.nrows = std::min(B.len, qmax - bpos + 1);
+            r.flags = (bpos + r.nrows - 1 > qmin) ? kRangeMasked : 0;
           } else {
             r.nrows = B.len;
             r.flags = 0;
@@ -193,17 +230,18 @@ Plan build_bwd_plan(const cp_desc_t* d, const ShardMap& m) {
           const Chunk& A = m.at(rho, B.seq, k);
           if (A.len == 0) continue;
           RangeDesc r{};
+          const int32_t apos = query_pos0(m, A, B);
           if (causal) {
-            if (A.pos0 + A.len - 1 < kmin) continue;  // every query precedes the keys
-            const int32_t skip = std::max(0, kmin - A.pos0);
+            if (apos + A.len - 1 < kmin) continue;  // every query precedes the keys
+            const int32_t skip = std::max(0, kmin - apos);
             r.row0 = int32_t(A.srow0 + skip);
             r.nrows = A.len - skip;
-            r.pos0 = A.pos0 + skip;
+            r.pos0 = apos + skip;
             r.flags = (r.pos0 < kmax) ? kRangeMasked : 0;
           } else {
             r.row0 = int32_t(A.srow0);
             r.nrows = A.len;
-            r.pos0 = A.pos0;
+            r.pos0 = apos;
             r.flags = 0;
           }
           work += ceil_tiles(r.nrows);
@@ -385,8 +423,10 @@ cp_status_t cp_workspace_size(const cp_desc_t* d, int32_t op, size_t* bytes) {
   if (op == CP_OP_PERMUTE) {
     cp_status_t st = check_map_fields(d);
     if (st != CP_OK) return st;
-    const size_t nseg = size_t(d->cp_size) * d->num_seqs * (d->layout == CP_LAYOUT_ZIGZAG ? 2 : 1);
-    *bytes = align256(nseg * sizeof(CopySeg));
+    const size_t nseg = d->layout == CP_LAYOUT_STRIPED
+                            ? size_t(d->total_tokens)
+                            : size_t(d->cp_size) * d->num_seqs * (d->layout == CP_LAYOUT_ZIGZAG ? 2 : 1);
+    *bytes = align256(std::max<size_t>(nseg, 1) * sizeof(CopySeg));
     return CP_OK;
   }
   cp_status_t st = check_attn_fields(d);
@@ -452,16 +492,23 @@ cp_status_t cp_shard_permute(const cp_desc_t* d, const void* in, void* out, int6
   std::vector<CopySeg> segs;
   segs.reserve(m.chunks.size());
   int64_t pieces = 0;
-  for (const Chunk& c : m.chunks) {
-    if (c.len == 0) continue;
+  auto add_seg = [&](int64_t grow, int64_t srow, int64_t rows) {
     CopySeg s;
-    const int64_t g = c.grow0 * row_bytes, sh = c.srow0 * row_bytes;
+    const int64_t g = grow * row_bytes, sh = srow * row_bytes;
     s.src = inverse ? sh : g;
     s.dst = inverse ? g : sh;
-    s.bytes = int64_t(c.len) * row_bytes;
+    s.bytes = rows * row_bytes;
     s.piece0 = pieces;
     pieces += (s.bytes + kPermutePiece - 1) / kPermutePiece;
     segs.push_back(s);
+  };
+  for (const Chunk& c : m.chunks) {
+    if (c.len == 0) continue;
+    if (c.stride == 1) {
+      add_seg(c.grow0, c.srow0, c.len);
+    } else {  // striped: every token is its own segment
+      for (int32_t i = 0; i < c.len; ++i) add_seg(c.grow0 + int64_t(i) * c.stride, c.srow0 + i, 1);
+    }
   }
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
   if (cudaMemcpyAsync(ws, segs.data(), segs.size() * sizeof(CopySeg), cudaMemcpyHostToDevice, cs) !=

@@ -17,8 +17,9 @@
  *     pieces, described by cu_seqlens).
  *   - "LLM context parallel production guide" (oh-bug.com), sections
  *     "核心原理" (exact merge through softmax statistics), "因果 Attention 会
- *     制造 Rank 负载不均" (skip blocks above the diagonal; zigzag balances the
- *     ranks; count effective QK blocks per rank), "变长序列" and
+ *     制造 Rank 负载不均" (skip blocks above the diagonal; zigzag or striped
+ *     placement balances the ranks; count effective QK blocks per rank),
+ *     "变长序列" and
  *     "位置编码必须跟序列分片一起走" (all position metadata follows the shard map).
  *
  * Conventions shared by every entry point
@@ -37,7 +38,11 @@
  *   - Shard map: sequence s of length L is cut into n pieces at floor(j*L/n),
  *     j = 0..n (pieces differ by at most one token and may be empty).
  *     CONTIGUOUS: n = C, rank r holds piece r.  ZIGZAG: n = 2C, rank r holds
- *     piece r then piece 2C-1-r.  Inside a rank, sequences appear in order.
+ *     piece r then piece 2C-1-r.  STRIPED: rank r holds the tokens at
+ *     positions p with p mod C == r, in increasing position ("LLM context
+ *     parallel production guide", 因果 Attention 会制造 Rank 负载不均:
+ *     striped token placement; one-token stripes).  Inside a rank, sequences
+ *     appear in order.
  *   - Layouts (row-major, innermost last):
  *       q [T, hq, d_qk]   k [T, hkv, d_qk]   v [T, hkv, d_v]
  *       o, dout [T, hq, d_v]   dq [T, hq, d_qk]   dk [T, hkv, d_qk]   dv [T, hkv, d_v]
@@ -79,7 +84,7 @@ typedef enum {
   CP_ERR_WORKSPACE = 5       /* workspace pointer NULL/misaligned or too small   */
 } cp_status_t;
 
-typedef enum { CP_LAYOUT_CONTIGUOUS = 0, CP_LAYOUT_ZIGZAG = 1 } cp_layout_t;
+typedef enum { CP_LAYOUT_CONTIGUOUS = 0, CP_LAYOUT_ZIGZAG = 1, CP_LAYOUT_STRIPED = 2 } cp_layout_t;
 typedef enum { CP_DT_F32 = 0, CP_DT_BF16 = 1 } cp_dtype_t;
 typedef enum { CP_GQA_BLOCKED = 0, CP_GQA_INTERLEAVED = 1 } cp_gqa_t;
 typedef enum {

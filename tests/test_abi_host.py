@@ -71,7 +71,7 @@ def test_null_descriptor_and_workspace_errors():
         cpa.cp_workspace_size(_prob(hq=3, hkv=2), cpa.CP_OP_FWD)
 
 
-@pytest.mark.parametrize("layout", ["contiguous", "zigzag"])
+@pytest.mark.parametrize("layout", ["contiguous", "zigzag", "striped"])
 @pytest.mark.parametrize("lengths", [[1000], [1, 2, 7, 64, 65, 300, 5], [4096, 31, 4097]])
 @pytest.mark.parametrize("C", [1, 2, 3, 8])
 def test_shard_offsets_match_oracle(layout, lengths, C):
@@ -121,6 +121,47 @@ def test_rank_block_counts(layout):
     cu = workloads.make_cu_seqlens(lengths).tolist()
     p = _prob(total_tokens=cu[-1], cu_seqlens=cu, cp_size=4, layout=layout)
     assert cpa.cp_rank_block_counts(p) == _tile_pairs_oracle(cu, 4, layout)
+
+
+def _striped_tile_pairs(cu, C):
+    """Visible (query tile, key tile) pairs per rank for striped shards, from
+    global positions: rank r holds positions r, r + C, ...; a query tile of
+    shard rows [t0, t1) ends at position r + C*(t1 - 1), and rank rho
+    contributes its tokens at positions <= that, cut into 128-row tiles."""
+    counts = []
+    for r in range(C):
+        tot = 0
+        for s in range(len(cu) - 1):
+            L = cu[s + 1] - cu[s]
+            n_r = len(oracle.striped_rows(L, C, r))
+            for t0 in range(0, n_r, 128):
+                last = r + C * (min(t0 + 128, n_r) - 1)
+                for rho in range(C):
+                    n_rho = len(oracle.striped_rows(L, C, rho))
+                    if last < rho or n_rho == 0:
+                        continue
+                    vis = min(n_rho, (last - rho) // C + 1)
+                    tot += -(-vis // 128)
+        counts.append(tot)
+    return counts
+
+
+def test_rank_block_counts_striped():
+    cu = [0, 8192]
+    p = _prob(total_tokens=8192, cu_seqlens=cu, cp_size=4, layout="striped")
+    got = cpa.cp_rank_block_counts(p)
+    assert got == _striped_tile_pairs(cu, 4)
+    assert max(got) - min(got) <= 3  # striped balances the causal work
+    lengths = workloads.varlen_lengths(20000, 64, 4000, 3)
+    cu = workloads.make_cu_seqlens(lengths).tolist()
+    p = _prob(total_tokens=cu[-1], cu_seqlens=cu, cp_size=4, layout="striped")
+    assert cpa.cp_rank_block_counts(p) == _striped_tile_pairs(cu, 4)
+
+
+def test_striped_permute_workspace_is_one_segment_per_token():
+    cu = [0, 100, 103]
+    p = _prob(total_tokens=103, cu_seqlens=cu, cp_size=4, layout="striped")
+    assert cpa.cp_workspace_size(p, cpa.CP_OP_PERMUTE) >= 103 * 32
 
 
 def test_workspace_sizes_positive_and_ordered():

@@ -30,6 +30,8 @@ CASES = [
     ([1, 2, 7, 64, 65, 300, 5], 8, "contiguous"),
     (workloads.varlen_lengths(30000, 64, 9000, 11), 16, "zigzag"),
     ([5], 8, "zigzag"),  # sequence shorter than 2C: empty chunks
+    ([1000], 4, "striped"),
+    ([1, 2, 7, 64, 65, 300, 5], 8, "striped"),  # sequences shorter than C: ranks without tokens
 ]
 
 

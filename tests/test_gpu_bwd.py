@@ -43,6 +43,7 @@ def _run(w: workloads.Workload, gqa="blocked"):
 F32_CASES = [
     dict(total_tokens=256, hq=2, hkv=2, d_qk=64, d_v=64, cp_size=2, layout="contiguous"),
     dict(total_tokens=300, hq=4, hkv=2, d_qk=64, d_v=64, cp_size=4, layout="zigzag", seqlens=(100, 1, 199)),
+    dict(total_tokens=300, hq=2, hkv=1, d_qk=64, d_v=64, cp_size=4, layout="striped", seqlens=(150, 2, 148)),
 ]
 
 
@@ -63,6 +64,9 @@ BF16_CASES = [
     # MLA-shaped heads with GQA and a ragged varlen pack (64-row query steps)
     dict(total_tokens=2000, hq=4, hkv=2, d_qk=192, d_v=128, cp_size=4, layout="zigzag", sigma=0.5,
          seqlens=(1300, 5, 695)),
+    # striped shards (shifted-diagonal blocks), varlen, both head widths
+    dict(total_tokens=3000, hq=4, hkv=2, d_qk=128, d_v=128, cp_size=4, layout="striped", seqlens=(1700, 3, 1297)),
+    dict(total_tokens=1500, hq=2, hkv=1, d_qk=192, d_v=128, cp_size=8, layout="striped", sigma=0.5),
 ]
 
 

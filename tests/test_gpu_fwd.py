@@ -51,6 +51,7 @@ F32_CASES = [
     dict(total_tokens=300, hq=4, hkv=2, d_qk=64, d_v=64, cp_size=4, layout="zigzag"),
     dict(total_tokens=500, hq=3, hkv=1, d_qk=32, d_v=64, cp_size=2, layout="contiguous", seqlens=(120, 1, 379)),
     dict(total_tokens=257, hq=2, hkv=2, d_qk=128, d_v=128, cp_size=8, layout="zigzag", causal=False),
+    dict(total_tokens=700, hq=4, hkv=2, d_qk=64, d_v=64, cp_size=4, layout="striped", seqlens=(300, 3, 397)),
 ]
 
 
@@ -74,6 +75,10 @@ BF16_CASES = [
     dict(total_tokens=1000, hq=2, hkv=1, d_qk=128, d_v=128, cp_size=1, layout="contiguous", causal=False),
     # MLA-shaped heads: 192-wide q/k, 128-wide v
     dict(total_tokens=2048, hq=2, hkv=2, d_qk=192, d_v=128, cp_size=4, layout="zigzag", sigma=0.5),
+    # striped shards: every (q rank, kv rank) block is a shifted causal diagonal
+    dict(total_tokens=4096, hq=4, hkv=1, d_qk=128, d_v=128, cp_size=4, layout="striped"),
+    dict(total_tokens=5000, hq=4, hkv=2, d_qk=128, d_v=128, cp_size=8, layout="striped",
+         seqlens=(2500, 7, 1200, 1293)),
 ]
 
 
@@ -103,7 +108,7 @@ def test_bf16_varlen_pack():
 
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
-@pytest.mark.parametrize("layout", ["zigzag", "contiguous"])
+@pytest.mark.parametrize("layout", ["zigzag", "contiguous", "striped"])
 def test_stepwise_ring_equals_oracle(dtype, layout):
     # Each virtual rank: block (r, r), then (r, r-1), ... merged in ring
     # order with cp_lse_merge ("Ulysses与Ring-Attention详解" §4.1-§4.2).
@@ -161,5 +166,7 @@ def test_layouts_agree_after_unpermute():
     oz, lz, _, _ = _run_fwd(workloads.Workload(name="z", cp_size=4, layout="zigzag", **base))
     oc, lc, _, _ = _run_fwd(workloads.Workload(name="c", cp_size=4, layout="contiguous", **base))
     o1, l1, _, _ = _run_fwd(workloads.Workload(name="one", cp_size=1, layout="contiguous", **base))
+    os_, ls, _, _ = _run_fwd(workloads.Workload(name="s", cp_size=4, layout="striped", **base))
     assert max_abs(oz, oc) < 2 * BF16_O_ATOL and max_abs(oz, o1) < 2 * BF16_O_ATOL
     assert max_abs(lz, lc) < 2 * BF16_LSE_ATOL and max_abs(lz, l1) < 2 * BF16_LSE_ATOL
+    assert max_abs(os_, o1) < 2 * BF16_O_ATOL and max_abs(ls, l1) < 2 * BF16_LSE_ATOL

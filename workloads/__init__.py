@@ -44,7 +44,7 @@ class Workload:
     hq, hkv      : query / key-value head counts (hq % hkv == 0)
     d_qk, d_v    : head dims of q/k and of v/o
     cp_size      : number of context-parallel shards C
-    layout       : "contiguous" or "zigzag"
+    layout       : "contiguous", "zigzag" or "striped"
     dtype        : "f32" or "bf16"
     sigma        : standard deviation of the N(0, sigma^2) inputs
     seed         : generator seed
