@@ -20,6 +20,10 @@ Contents and the passage each follows:
   striped placement, and the per-rank visible-pair counts.  "Ulysses与Ring-Attention详解" §4.2 (zigzag pairs block i with
   block 2C-1-i); "超长上下文训练速度翻倍秘籍" §3 varlen CP (every sub-sequence
   is itself cut into CP pieces).
+* ``ulysses``    — the all-to-all re-layout of Ulysses CP on one device
+  (sequence shards <-> head shards).  "Ulysses Context Parallelism
+  的工程取舍全记录" §1.2, §2 (GQA: C divides the KV head count);
+  "超长上下文训练速度翻倍秘籍", All2All CP 实现.
 * ``merge``      — the exact log-sum-exp merge of two partial results.
   "Ulysses与Ring-Attention详解" §4.2 (lse_new = log(exp(lse_prev) +
   exp(lse_cur))); "LLM context parallel production guide" "核心原理" (partials
@@ -48,3 +52,9 @@ from .sharding import (  # noqa: F401
     to_global,
 )
 from .merge import lse_merge  # noqa: F401
+from .ulysses import (  # noqa: F401
+    ulysses_scatter,
+    ulysses_gather,
+    ulysses_scatter_lse,
+    ulysses_gather_lse,
+)
