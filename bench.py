@@ -241,6 +241,50 @@ class Runner:
         return statistics.mean(fwd), statistics.mean(bwd), statistics.mean(dkdv), statistics.mean(dq)
 
 
+def ulysses_measure(r: Runner, steps: int = 3, warmup: int = 2) -> dict:
+    """The step's attention computed the Ulysses way on the same sharded
+    inputs (all-to-all, full-sequence attention of every rank's heads,
+    all-to-all back: cp_ulysses_attn_fwd / _bwd), device time per step, and
+    the bandwidth of one all-to-all re-layout of q (read + write)."""
+    cpa, w = r.cpa, r.w
+    try:
+        ws_f = cpa.workspace(r.prob, cpa.CP_OP_ULYSSES_FWD, r.dev)
+        ws_b = cpa.workspace(r.prob, cpa.CP_OP_ULYSSES_BWD, r.dev)
+    except cpa.CpError as e:
+        return {"unavailable": str(e)}
+    s = r.s
+    times = []
+    for i in range(warmup + steps):
+        e = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+        e[0].record()
+        cpa.cp_ulysses_attn_fwd(r.prob, s["q"], s["k"], s["v"], r.o, r.lse, ws_f)
+        e[1].record()
+        cpa.cp_ulysses_attn_bwd(r.prob, s["q"], s["k"], s["v"], r.o, r.lse, s["dout"], r.dq, r.dk, r.dv, ws_b)
+        e[2].record()
+        if i >= warmup:
+            times.append(e)
+    torch.cuda.synchronize()
+    if cpa.cp_device_status() != 0:
+        raise RuntimeError("device wait timeout in the Ulysses path")
+    fwd = statistics.mean(a.elapsed_time(b) for a, b, _ in times)
+    bwd = statistics.mean(b.elapsed_time(c) for _, b, c in times)
+    del ws_f, ws_b
+    # one re-layout of q: T*hq*d_qk bf16 read and written
+    u = torch.empty(w.cp_size, w.total_tokens, w.hq // w.cp_size, w.d_qk, dtype=torch.bfloat16, device=r.dev)
+    ws_a = cpa.workspace(r.prob, cpa.CP_OP_ULYSSES_A2A, r.dev)
+    best = float("inf")
+    for _ in range(6):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        cpa.cp_ulysses_a2a(r.prob, s["q"], out=u, ws=ws_a)
+        b.record()
+        torch.cuda.synchronize()
+        best = min(best, a.elapsed_time(b))
+    nbytes = 2 * s["q"].numel() * 2
+    return {"fwd_ms": round(fwd, 3), "bwd_ms": round(bwd, 3), "ms_per_step": round(fwd + bwd, 3),
+            "a2a_q": {"bytes": nbytes, "ms": round(best, 4), "gbs": round(nbytes / (best * 1e-3) / 1e9, 1)}}
+
+
 def e2e_measure(r: Runner, steps: int, warmup: int):
     """Same metric through the ABI with host buffers: pinned host inputs are
     copied in, the step runs, and o, dq, dk, dv are copied back each step."""
@@ -359,6 +403,7 @@ def run_gpu(args):
 
     e2e_ms, h2d, d2h = e2e_measure(r, max(1, min(args.steps, 3)), 1)
     aux = aux_bandwidth(r)
+    uly = ulysses_measure(r) if not args.no_ulysses else {"skipped": "--no-ulysses"}
 
     peaks, peak_kind = load_peaks()
     peak_sus = float(peaks.get("bf16_tflops_sustained", FALLBACK["bf16_tflops_sustained"]))
@@ -420,7 +465,13 @@ def run_gpu(args):
             "gpu_launches": r.launches_per_step * args.steps,
             "rank_block_counts": cpa.cp_rank_block_counts(r.prob),
             "rank_balance": balance_report(cpa, w),
+            "ulysses": uly,
         }
+        if "ms_per_step" in uly:
+            hbm = float(peaks.get("hbm_gbs", FALLBACK["hbm_gbs"]))
+            uly["tflops"] = round((f_fwd + f_bwd) / (uly["ms_per_step"] * 1e-3) / 1e12, 2)
+            uly["ring_attention_ms_per_step"] = round(fwd_ms + bwd_ms, 3)
+            uly["a2a_q"]["frac"] = round(uly["a2a_q"]["gbs"] / hbm, 4)
         if not args.no_cpu_baseline:
             tf, secs, desc = oracle_sample(w, args.cpu_tokens)
             result["cpu_baseline"] = {"value": round(tf, 6), "unit": "TFLOP/s", "cores": cpu_cores(),
@@ -481,6 +532,7 @@ def main():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=list(workloads.WORKLOADS))
     ap.add_argument("--cpu-tokens", type=int, default=8192)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-ulysses", action="store_true", help="skip the Ulysses comparison")
     ap.add_argument("--layout", default=None, choices=["contiguous", "zigzag", "striped"],
                     help="shard layout instead of the workload's own (zigzag for the standard ones)")
     args = ap.parse_args()

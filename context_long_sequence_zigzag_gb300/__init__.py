@@ -12,7 +12,8 @@ a non-OK status.
 Functions carry the C names: ``cp_shard_permute``, ``cp_attn_block_fwd``,
 ``cp_lse_merge``, ``cp_attn_fwd``, ``cp_attn_bwd``, ``cp_workspace_size``,
 ``cp_shard_offsets``, ``cp_rank_block_counts``, ``cp_device_status``,
-``cp_check_bounded_wait``, ``cp_status_string``, ``cp_validate``.
+``cp_check_bounded_wait``, ``cp_status_string``, ``cp_validate``, ``cp_ulysses_a2a``,
+``cp_ulysses_attn_fwd``, ``cp_ulysses_attn_bwd``.
 """
 
 from __future__ import annotations
@@ -39,12 +40,14 @@ CP_LAYOUT_CONTIGUOUS, CP_LAYOUT_ZIGZAG, CP_LAYOUT_STRIPED = 0, 1, 2
 CP_DT_F32, CP_DT_BF16 = 0, 1
 CP_GQA_BLOCKED, CP_GQA_INTERLEAVED = 0, 1
 CP_OP_FWD, CP_OP_BWD, CP_OP_BLOCK_FWD, CP_OP_PERMUTE, CP_OP_BWD_DKDV, CP_OP_BWD_DQ = 0, 1, 2, 3, 4, 5
+CP_OP_ULYSSES_A2A, CP_OP_ULYSSES_FWD, CP_OP_ULYSSES_BWD = 6, 7, 8
 
 EXPORTED = [
     "cp_status_string", "cp_validate", "cp_workspace_size", "cp_shard_offsets",
     "cp_rank_block_counts", "cp_shard_permute", "cp_attn_block_fwd", "cp_lse_merge",
     "cp_attn_fwd", "cp_attn_bwd", "cp_device_status", "cp_check_bounded_wait",
     "cp_attn_fwd_noalloc", "cp_attn_bwd_prep", "cp_attn_bwd_dkdv", "cp_attn_bwd_dq",
+    "cp_ulysses_a2a", "cp_ulysses_attn_fwd", "cp_ulysses_attn_bwd",
 ]
 
 
@@ -86,6 +89,10 @@ _sigs = {
     "cp_attn_bwd_prep": (ctypes.c_int, [_DP, _P, _P, _P, _P]),
     "cp_attn_bwd_dkdv": (ctypes.c_int, [_DP, _P, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
     "cp_attn_bwd_dq": (ctypes.c_int, [_DP, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
+    "cp_ulysses_a2a": (ctypes.c_int, [_DP, _P, _P, ctypes.c_int32, ctypes.c_int64, ctypes.c_int32, _P,
+                                      ctypes.c_size_t, _P]),
+    "cp_ulysses_attn_fwd": (ctypes.c_int, [_DP, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
+    "cp_ulysses_attn_bwd": (ctypes.c_int, [_DP, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
 }
 for _name, (_res, _args) in _sigs.items():
     _f = getattr(_lib, _name)
@@ -261,6 +268,57 @@ def cp_attn_bwd(prob: Problem, q, k, v, o, lse, dout, dq=None, dk=None, dv=None,
         ws = workspace(prob, CP_OP_BWD, q.device)
     _check(_lib.cp_attn_bwd(prob.ptr, _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout), _ptr(dq),
                             _ptr(dk), _ptr(dv), _ptr(ws), ws.numel(), _stream(stream)), "cp_attn_bwd")
+    return dq, dk, dv
+
+
+def cp_ulysses_a2a(prob: Problem, x: torch.Tensor, inverse: bool = False, out: Optional[torch.Tensor] = None,
+                   ws: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """Ulysses all-to-all re-layout.  Forward: x [T, H, ...] in sharded order
+    -> [C, T, H/C, ...] (rank r: heads r*H/C.., global token order).
+    Inverse: [C, T, H/C, ...] -> [T, H, ...] sharded."""
+    C = prob.desc.cp_size
+    if inverse:
+        heads = x.shape[2] * C
+        shape = (x.shape[1], heads) + tuple(x.shape[3:])
+    else:
+        heads = x.shape[1]
+        shape = (C, x.shape[0], heads // C) + tuple(x.shape[2:])
+    head_bytes = (x[0, 0].numel() if not inverse else x[0, 0, 0].numel()) * x.element_size()
+    if out is None:
+        out = torch.empty(shape, dtype=x.dtype, device=x.device)
+    if ws is None:
+        ws = workspace(prob, CP_OP_ULYSSES_A2A, x.device)
+    _check(_lib.cp_ulysses_a2a(prob.ptr, _ptr(x), _ptr(out), heads, head_bytes, int(bool(inverse)), _ptr(ws),
+                               ws.numel(), _stream(stream)), "cp_ulysses_a2a")
+    return out
+
+
+def cp_ulysses_attn_fwd(prob: Problem, q, k, v, o=None, lse=None, ws=None, stream=None):
+    """cp_attn_fwd computed the Ulysses way (all-to-all, per-rank full-sequence
+    attention, all-to-all back); same inputs and outputs."""
+    d = prob.desc
+    if o is None:
+        o = torch.empty(d.total_tokens, d.hq, d.d_v, dtype=q.dtype, device=q.device)
+    if lse is None:
+        lse = torch.empty(d.hq, d.total_tokens, dtype=torch.float32, device=q.device)
+    if ws is None:
+        ws = workspace(prob, CP_OP_ULYSSES_FWD, q.device)
+    _check(_lib.cp_ulysses_attn_fwd(prob.ptr, _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(ws), ws.numel(),
+                                    _stream(stream)), "cp_ulysses_attn_fwd")
+    return o, lse
+
+
+def cp_ulysses_attn_bwd(prob: Problem, q, k, v, o, lse, dout, dq=None, dk=None, dv=None, ws=None, stream=None):
+    if dq is None:
+        dq = torch.empty_like(q)
+    if dk is None:
+        dk = torch.empty_like(k)
+    if dv is None:
+        dv = torch.empty_like(v)
+    if ws is None:
+        ws = workspace(prob, CP_OP_ULYSSES_BWD, q.device)
+    _check(_lib.cp_ulysses_attn_bwd(prob.ptr, _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout), _ptr(dq),
+                                    _ptr(dk), _ptr(dv), _ptr(ws), ws.numel(), _stream(stream)), "cp_ulysses_attn_bwd")
     return dq, dk, dv
 
 

@@ -356,6 +356,86 @@ struct BwdLayout {
   size_t fwd_plan, bwd_plan, dpsum, total;
 };
 
+// ---------------------------------------------------------------- Ulysses
+// "Ulysses Context Parallelism 的工程取舍全记录" §1.2 / §2: the all-to-all hands
+// rank r heads r*H/C .. (r+1)*H/C - 1 of the whole sequence; with GQA every
+// rank needs whole KV heads, so C must divide hq and hkv (blocked GQA keeps a
+// rank's query heads on its own KV heads).
+cp_status_t check_ulysses(const cp_desc_t* d) {
+  const int C = d->cp_size;
+  if (d->hq % C != 0 || d->hkv % C != 0) return CP_ERR_UNSUPPORTED;
+  if (d->gqa != CP_GQA_BLOCKED && d->hq != d->hkv) return CP_ERR_UNSUPPORTED;
+  if (int64_t(C) * d->total_tokens > INT32_MAX) return CP_ERR_UNSUPPORTED;
+  return CP_OK;
+}
+
+// Global row of every sharded row (the shard map's permutation).
+std::vector<int32_t> sharded_to_global(const ShardMap& m, int64_t T) {
+  std::vector<int32_t> perm(static_cast<size_t>(T));
+  for (const Chunk& c : m.chunks)
+    for (int32_t i = 0; i < c.len; ++i) perm[size_t(c.srow0 + i)] = int32_t(c.grow0 + int64_t(i) * c.stride);
+  return perm;
+}
+
+// The C per-rank unsharded problems as one problem: rank r's block of the
+// head-sharded tensors is a copy of the whole sequence set (rows r*T ..),
+// with H/C heads; cp_size 1 (full-sequence attention, the pages' "完整
+// FlashAttention" per device).
+struct UlyssesProblem {
+  cp_desc_t u;
+  std::vector<int32_t> cu;
+};
+UlyssesProblem ulysses_problem(const cp_desc_t* d) {
+  UlyssesProblem p;
+  const std::vector<int32_t> cu = seqlens_of(d);
+  const int C = d->cp_size;
+  p.cu.push_back(0);
+  for (int r = 0; r < C; ++r)
+    for (size_t s = 1; s < cu.size(); ++s) p.cu.push_back(int32_t(int64_t(r) * d->total_tokens + cu[s]));
+  p.u = *d;
+  p.u.total_tokens = int64_t(C) * d->total_tokens;
+  p.u.num_seqs = C * (int32_t(cu.size()) - 1);
+  p.u.cu_seqlens = p.cu.data();
+  p.u.hq = d->hq / C;
+  p.u.hkv = d->hkv / C;
+  p.u.cp_size = 1;
+  p.u.layout = CP_LAYOUT_CONTIGUOUS;
+  return p;
+}
+
+// Workspace of the Ulysses attention calls: the row map, the head-sharded
+// copies of the tensors and the inner call's own workspace.
+struct UlyssesLayout {
+  size_t perm, q, k, v, o, dout, dq, dk, dv, lse, inner, inner_bytes, total;
+};
+UlyssesLayout ulysses_layout(const cp_desc_t* d, const cp_desc_t& u, bool bwd) {
+  const size_t elt = d->dtype == CP_DT_BF16 ? 2 : 4;
+  const size_t T = size_t(d->total_tokens);
+  const size_t nq = align256(T * d->hq * d->d_qk * elt), nk = align256(T * d->hkv * d->d_qk * elt);
+  const size_t nv = align256(T * d->hkv * d->d_v * elt), no = align256(T * d->hq * d->d_v * elt);
+  UlyssesLayout L{};
+  size_t off = 0;
+  auto take = [&](size_t n) { const size_t at = off; off += n; return at; };
+  L.perm = take(align256(T * 4));
+  L.q = take(nq);
+  L.k = take(nk);
+  L.v = take(nv);
+  L.o = take(no);
+  L.lse = take(align256(T * d->hq * 4));
+  if (bwd) {
+    L.dout = take(no);
+    L.dq = take(nq);
+    L.dk = take(nk);
+    L.dv = take(nv);
+  }
+  size_t inner = 0;
+  cp_workspace_size(&u, bwd ? CP_OP_BWD : CP_OP_FWD, &inner);
+  L.inner = take(align256(inner));
+  L.inner_bytes = align256(inner);
+  L.total = off;
+  return L;
+}
+
 BwdLayout bwd_layout(const cp_desc_t* d, const Plan& pf, const Plan& pb) {
   BwdLayout L{};
   L.fwd_plan = 0;
@@ -420,6 +500,12 @@ cp_status_t cp_validate(const cp_desc_t* d) { return check_attn_fields(d); }
 
 cp_status_t cp_workspace_size(const cp_desc_t* d, int32_t op, size_t* bytes) {
   if (bytes == nullptr) return CP_ERR_INVALID_ARG;
+  if (op == CP_OP_ULYSSES_A2A) {
+    cp_status_t st = check_map_fields(d);
+    if (st != CP_OK) return st;
+    *bytes = align256(std::max<size_t>(size_t(d->total_tokens), 1) * 4);
+    return CP_OK;
+  }
   if (op == CP_OP_PERMUTE) {
     cp_status_t st = check_map_fields(d);
     if (st != CP_OK) return st;
@@ -446,6 +532,11 @@ cp_status_t cp_workspace_size(const cp_desc_t* d, int32_t op, size_t* bytes) {
     *bytes = plan_bytes(build_bwd_plan(d, m));
   } else if (op == CP_OP_BWD_DQ) {
     *bytes = plan_bytes(build_fwd_plan(d, m, -1, -1));
+  } else if (op == CP_OP_ULYSSES_FWD || op == CP_OP_ULYSSES_BWD) {
+    st = check_ulysses(d);
+    if (st != CP_OK) return st;
+    const UlyssesProblem up = ulysses_problem(d);
+    *bytes = ulysses_layout(d, up.u, op == CP_OP_ULYSSES_BWD).total;
   } else {
     return CP_ERR_INVALID_ARG;
   }
@@ -695,6 +786,108 @@ cp_status_t cp_attn_fwd_noalloc(const cp_desc_t* d, const void* q, const void* k
   a.lse = lse;
   cudaError_t e = use_tc_fwd(d) ? launch_tc_fwd(a, cs) : launch_simt_fwd(a, d->dtype, cs);
   return e == cudaSuccess ? CP_OK : CP_ERR_CUDA;
+}
+
+cp_status_t cp_ulysses_a2a(const cp_desc_t* d, const void* in, void* out, int32_t heads, int64_t head_bytes,
+                           int32_t inverse, void* ws, size_t ws_bytes, cp_stream_t stream) {
+  cp_status_t st = check_map_fields(d);
+  if (st != CP_OK) return st;
+  if (heads < 1 || heads % d->cp_size != 0 || head_bytes <= 0 || head_bytes % 16 != 0) return CP_ERR_INVALID_ARG;
+  if (inverse != 0 && inverse != 1) return CP_ERR_INVALID_ARG;
+  if (d->total_tokens == 0) return CP_OK;
+  if (in == nullptr || out == nullptr || !aligned16(in) || !aligned16(out)) return CP_ERR_INVALID_ARG;
+  const int64_t total = d->total_tokens * heads * head_bytes;
+  const char* ib = static_cast<const char*>(in);
+  const char* ob = static_cast<const char*>(out);
+  if (ib < ob + total && ob < ib + total) return CP_ERR_INVALID_ARG;  // overlap
+  const size_t need = align256(size_t(d->total_tokens) * 4);
+  if (ws == nullptr || (reinterpret_cast<uintptr_t>(ws) & 255) || ws_bytes < need) return CP_ERR_WORKSPACE;
+  const std::vector<int32_t> perm = sharded_to_global(build_map(d), d->total_tokens);
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  if (cudaMemcpyAsync(ws, perm.data(), perm.size() * 4, cudaMemcpyHostToDevice, cs) != cudaSuccess) return CP_ERR_CUDA;
+  const int64_t chunk = int64_t(heads / d->cp_size) * head_bytes;
+  return launch_ulysses_a2a(static_cast<const int32_t*>(ws), d->total_tokens, d->cp_size, chunk, in, out, inverse,
+                            cs) == cudaSuccess
+             ? CP_OK
+             : CP_ERR_CUDA;
+}
+
+cp_status_t cp_ulysses_attn_fwd(const cp_desc_t* d, const void* q, const void* k, const void* v, void* o,
+                                float* lse, void* ws, size_t ws_bytes, cp_stream_t stream) {
+  cp_status_t st = check_attn_fields(d);
+  if (st != CP_OK) return st;
+  st = check_ulysses(d);
+  if (st != CP_OK) return st;
+  if (d->total_tokens == 0) return CP_OK;
+  const void* ptrs[] = {q, k, v, o, lse};
+  for (const void* p : ptrs)
+    if (p == nullptr || !aligned16(p)) return CP_ERR_INVALID_ARG;
+  const UlyssesProblem up = ulysses_problem(d);
+  const UlyssesLayout L = ulysses_layout(d, up.u, false);
+  if (ws == nullptr || (reinterpret_cast<uintptr_t>(ws) & 255) || ws_bytes < L.total) return CP_ERR_WORKSPACE;
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  char* base = static_cast<char*>(ws);
+  const int32_t* perm = reinterpret_cast<const int32_t*>(base + L.perm);
+  const std::vector<int32_t> hperm = sharded_to_global(build_map(d), d->total_tokens);
+  if (cudaMemcpyAsync(base + L.perm, hperm.data(), hperm.size() * 4, cudaMemcpyHostToDevice, cs) != cudaSuccess)
+    return CP_ERR_CUDA;
+  const int64_t T = d->total_tokens;
+  const int C = d->cp_size, elt = d->dtype == CP_DT_BF16 ? 2 : 4;
+  // all-to-all #1: sequence shards -> head shards
+  if (launch_ulysses_a2a(perm, T, C, int64_t(d->hq / C) * d->d_qk * elt, q, base + L.q, 0, cs) != cudaSuccess ||
+      launch_ulysses_a2a(perm, T, C, int64_t(d->hkv / C) * d->d_qk * elt, k, base + L.k, 0, cs) != cudaSuccess ||
+      launch_ulysses_a2a(perm, T, C, int64_t(d->hkv / C) * d->d_v * elt, v, base + L.v, 0, cs) != cudaSuccess)
+    return CP_ERR_CUDA;
+  // full-sequence attention of every rank's heads
+  st = cp_attn_fwd(&up.u, base + L.q, base + L.k, base + L.v, base + L.o, reinterpret_cast<float*>(base + L.lse),
+                   base + L.inner, L.inner_bytes, stream);
+  if (st != CP_OK) return st;
+  // all-to-all #2: head shards -> sequence shards
+  if (launch_ulysses_a2a(perm, T, C, int64_t(d->hq / C) * d->d_v * elt, base + L.o, o, 1, cs) != cudaSuccess ||
+      launch_ulysses_lse(perm, T, C, d->hq, reinterpret_cast<const float*>(base + L.lse), lse, 1, cs) != cudaSuccess)
+    return CP_ERR_CUDA;
+  return CP_OK;
+}
+
+cp_status_t cp_ulysses_attn_bwd(const cp_desc_t* d, const void* q, const void* k, const void* v, const void* o,
+                                const float* lse, const void* dout, void* dq, void* dk, void* dv, void* ws,
+                                size_t ws_bytes, cp_stream_t stream) {
+  cp_status_t st = check_attn_fields(d);
+  if (st != CP_OK) return st;
+  st = check_ulysses(d);
+  if (st != CP_OK) return st;
+  if (d->total_tokens == 0) return CP_OK;
+  const void* ptrs[] = {q, k, v, o, lse, dout, dq, dk, dv};
+  for (const void* p : ptrs)
+    if (p == nullptr || !aligned16(p)) return CP_ERR_INVALID_ARG;
+  const UlyssesProblem up = ulysses_problem(d);
+  const UlyssesLayout L = ulysses_layout(d, up.u, true);
+  if (ws == nullptr || (reinterpret_cast<uintptr_t>(ws) & 255) || ws_bytes < L.total) return CP_ERR_WORKSPACE;
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  char* base = static_cast<char*>(ws);
+  const int32_t* perm = reinterpret_cast<const int32_t*>(base + L.perm);
+  const std::vector<int32_t> hperm = sharded_to_global(build_map(d), d->total_tokens);
+  if (cudaMemcpyAsync(base + L.perm, hperm.data(), hperm.size() * 4, cudaMemcpyHostToDevice, cs) != cudaSuccess)
+    return CP_ERR_CUDA;
+  const int64_t T = d->total_tokens;
+  const int C = d->cp_size, elt = d->dtype == CP_DT_BF16 ? 2 : 4;
+  const int64_t cq = int64_t(d->hq / C) * d->d_qk * elt, ck = int64_t(d->hkv / C) * d->d_qk * elt;
+  const int64_t cv = int64_t(d->hkv / C) * d->d_v * elt, co = int64_t(d->hq / C) * d->d_v * elt;
+  if (launch_ulysses_a2a(perm, T, C, cq, q, base + L.q, 0, cs) != cudaSuccess ||
+      launch_ulysses_a2a(perm, T, C, ck, k, base + L.k, 0, cs) != cudaSuccess ||
+      launch_ulysses_a2a(perm, T, C, cv, v, base + L.v, 0, cs) != cudaSuccess ||
+      launch_ulysses_a2a(perm, T, C, co, o, base + L.o, 0, cs) != cudaSuccess ||
+      launch_ulysses_a2a(perm, T, C, co, dout, base + L.dout, 0, cs) != cudaSuccess ||
+      launch_ulysses_lse(perm, T, C, d->hq, lse, reinterpret_cast<float*>(base + L.lse), 0, cs) != cudaSuccess)
+    return CP_ERR_CUDA;
+  st = cp_attn_bwd(&up.u, base + L.q, base + L.k, base + L.v, base + L.o, reinterpret_cast<const float*>(base + L.lse),
+                   base + L.dout, base + L.dq, base + L.dk, base + L.dv, base + L.inner, L.inner_bytes, stream);
+  if (st != CP_OK) return st;
+  if (launch_ulysses_a2a(perm, T, C, cq, base + L.dq, dq, 1, cs) != cudaSuccess ||
+      launch_ulysses_a2a(perm, T, C, ck, base + L.dk, dk, 1, cs) != cudaSuccess ||
+      launch_ulysses_a2a(perm, T, C, cv, base + L.dv, dv, 1, cs) != cudaSuccess)
+    return CP_ERR_CUDA;
+  return CP_OK;
 }
 
 cp_status_t cp_device_status(cp_stream_t stream, int32_t* code) {

@@ -89,6 +89,11 @@ enum : int32_t {
 // ---- launchers (each returns cudaSuccess or the launch error) ----
 cudaError_t launch_permute(const CopySeg* segs, int32_t nseg, int64_t npieces,
                            const void* in, void* out, cudaStream_t st);
+// Ulysses re-layout: perm[s] = global row of sharded row s (T entries, device).
+cudaError_t launch_ulysses_a2a(const int32_t* perm, int64_t T, int32_t C, int64_t chunk_bytes, const void* in,
+                               void* out, int32_t inverse, cudaStream_t st);
+cudaError_t launch_ulysses_lse(const int32_t* perm, int64_t T, int32_t C, int32_t H, const float* in, float* out,
+                               int32_t inverse, cudaStream_t st);
 cudaError_t launch_lse_merge(int64_t rows, int32_t hq, int32_t dv, float* o_acc, float* lse_acc,
                              const float* o_part, const float* lse_part, cudaStream_t st);
 cudaError_t launch_simt_fwd(const AttnArgs& a, int32_t dtype, cudaStream_t st);

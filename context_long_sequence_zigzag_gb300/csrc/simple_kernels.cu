@@ -61,6 +61,63 @@ __global__ void __launch_bounds__(kPermThreads) permute_kernel(const CopySeg* __
 }
 
 // ----------------------------------------------------------------------------
+// Ulysses all-to-all on one GPU ("Ulysses Context Parallelism 的工程取舍全记录"
+// §1.2): sequence shards of every head <-> the whole sequence of H/C heads
+// per virtual rank.  A sharded row s (token perm[s] in global order) holds C
+// consecutive head groups of chunk16 16-byte words; group r goes to row
+// perm[s] of rank r's [T, H/C, ...] block.  One warp per sharded row; the
+// direction only swaps which side is read.
+// ----------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) ulysses_a2a_kernel(const int32_t* __restrict__ perm, int64_t T,
+                                                          int32_t C, int64_t chunk16,
+                                                          const int4* __restrict__ in, int4* __restrict__ out,
+                                                          int32_t inverse) {
+  const int lane = threadIdx.x & 31;
+  const int64_t nwarps = int64_t(gridDim.x) * (blockDim.x >> 5);
+  for (int64_t s = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; s < T; s += nwarps) {
+    const int64_t g = perm[s];
+    const int64_t srow = s * C * chunk16;
+    for (int r = 0; r < C; ++r) {
+      const int64_t sh = srow + int64_t(r) * chunk16;    // sharded side
+      const int64_t uh = (int64_t(r) * T + g) * chunk16;  // head-sharded side
+      const int64_t src = inverse ? uh : sh, dst = inverse ? sh : uh;
+      for (int64_t i0 = 0; i0 < chunk16; i0 += 128) {
+        int4 buf[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int64_t i = i0 + lane + 32 * u;
+          if (i < chunk16) buf[u] = __ldcs(in + src + i);
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int64_t i = i0 + lane + 32 * u;
+          if (i < chunk16) __stcs(out + dst + i, buf[u]);
+        }
+      }
+    }
+  }
+}
+
+// Statistics [H, T] (sharded token order) <-> [H/C, C*T] (head h = r*H/C + j
+// of rank r at row j, column r*T + perm[s]): the layout of the unsharded
+// per-rank problem's lse.
+__global__ void __launch_bounds__(256) ulysses_lse_kernel(const int32_t* __restrict__ perm, int64_t T,
+                                                          int32_t C, int32_t H, const float* __restrict__ in,
+                                                          float* __restrict__ out, int32_t inverse) {
+  const int64_t n = int64_t(H) * T;
+  const int32_t hc = H / C;
+  for (int64_t e = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; e < n; e += int64_t(gridDim.x) * blockDim.x) {
+    const int64_t h = e / T, s = e - h * T;
+    const int64_t r = h / hc, j = h - r * hc;
+    const int64_t u = j * (C * T) + r * T + perm[s];
+    if (inverse)
+      out[e] = in[u];
+    else
+      out[u] = in[e];
+  }
+}
+
+// ----------------------------------------------------------------------------
 // LSE merge ("Ulysses与Ring-Attention详解" §4.1 update step, §4.2 lse formula).
 // One warp per (row, head): lse = max + log1p(exp(-|a-b|)), weights
 // exp(a - lse), exp(b - lse); -inf is the identity.
@@ -353,6 +410,21 @@ cudaError_t launch_permute(const CopySeg* segs, int32_t nseg, int64_t npieces, c
   permute_kernel<<<unsigned(grid), kPermThreads, 0, st>>>(segs, nseg, npieces,
                                                           static_cast<const char*>(in),
                                                           static_cast<char*>(out));
+  return cudaGetLastError();
+}
+
+cudaError_t launch_ulysses_a2a(const int32_t* perm, int64_t T, int32_t C, int64_t chunk_bytes, const void* in,
+                               void* out, int32_t inverse, cudaStream_t st) {
+  const int64_t grid = grid_for(T, 8);
+  ulysses_a2a_kernel<<<unsigned(grid), 256, 0, st>>>(perm, T, C, chunk_bytes / 16, static_cast<const int4*>(in),
+                                                     static_cast<int4*>(out), inverse);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_ulysses_lse(const int32_t* perm, int64_t T, int32_t C, int32_t H, const float* in, float* out,
+                               int32_t inverse, cudaStream_t st) {
+  const int64_t grid = grid_for(int64_t(H) * T, 256);
+  ulysses_lse_kernel<<<unsigned(grid), 256, 0, st>>>(perm, T, C, H, in, out, inverse);
   return cudaGetLastError();
 }
 

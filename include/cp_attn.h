@@ -88,7 +88,8 @@ typedef enum { CP_LAYOUT_CONTIGUOUS = 0, CP_LAYOUT_ZIGZAG = 1, CP_LAYOUT_STRIPED
 typedef enum { CP_DT_F32 = 0, CP_DT_BF16 = 1 } cp_dtype_t;
 typedef enum { CP_GQA_BLOCKED = 0, CP_GQA_INTERLEAVED = 1 } cp_gqa_t;
 typedef enum {
-  CP_OP_FWD = 0, CP_OP_BWD = 1, CP_OP_BLOCK_FWD = 2, CP_OP_PERMUTE = 3, CP_OP_BWD_DKDV = 4, CP_OP_BWD_DQ = 5
+  CP_OP_FWD = 0, CP_OP_BWD = 1, CP_OP_BLOCK_FWD = 2, CP_OP_PERMUTE = 3, CP_OP_BWD_DKDV = 4, CP_OP_BWD_DQ = 5,
+  CP_OP_ULYSSES_A2A = 6, CP_OP_ULYSSES_FWD = 7, CP_OP_ULYSSES_BWD = 8
 } cp_op_t;
 
 /* Problem descriptor.  Read on the host during each call; not retained. */
@@ -194,6 +195,53 @@ cp_status_t cp_attn_bwd(const cp_desc_t* desc, const void* q, const void* k, con
                         const void* o, const float* lse, const void* dout,
                         void* dq, void* dk, void* dv,
                         void* workspace, size_t workspace_bytes, cp_stream_t stream);
+
+/* ---------------------------------------------------------------- Ulysses
+ * All-to-all ("Ulysses") context parallelism with the C virtual ranks on one
+ * GPU ("Ulysses Context Parallelism 的工程取舍全记录" §1.2: before attention an
+ * all-to-all turns sequence shards of every head into the whole sequence of
+ * H/C heads per device, device r taking heads r*H/C .. (r+1)*H/C - 1; after
+ * attention a second all-to-all turns the output back; §2: with GQA every
+ * device needs whole KV heads, so C must divide hq and hkv;
+ * "超长上下文训练速度翻倍秘籍", All2All CP 实现).  On one GPU the all-to-all is
+ * a re-layout between
+ *   sharded   [T, H, e] in sharded token order (the layout of every other call), and
+ *   head-sharded [C, T, H/C, e]: rank r's block holds heads r*H/C.. of all T
+ *                tokens in GLOBAL token order (cu_seqlens order).
+ * e = bytes per head (head_bytes). */
+
+/* The all-to-all re-layout, bit-exact.
+ *   in, out    : device, T * heads * head_bytes bytes each, 16-byte aligned,
+ *                not overlapping
+ *   heads      : heads of this tensor (hq for q/o/dq, hkv for k/v/dk/dv);
+ *                must be a multiple of cp_size
+ *   head_bytes : bytes per head, > 0, multiple of 16
+ *   inverse    : 0 = sharded -> head-sharded, 1 = head-sharded -> sharded
+ *   workspace  : cp_workspace_size(desc, CP_OP_ULYSSES_A2A) bytes (the row map)
+ * Only total_tokens, num_seqs, cu_seqlens, cp_size and layout are read. */
+cp_status_t cp_ulysses_a2a(const cp_desc_t* desc, const void* in, void* out, int32_t heads,
+                           int64_t head_bytes, int32_t inverse,
+                           void* workspace, size_t workspace_bytes, cp_stream_t stream);
+
+/* Ulysses attention forward: the same inputs and outputs as cp_attn_fwd
+ * (sharded order, all heads), computed as all-to-all, full-sequence
+ * attention of every rank's heads (the tcgen05 kernels with one rank), and
+ * all-to-all back.  Results equal cp_attn_fwd's up to rounding order.
+ *   workspace : cp_workspace_size(desc, CP_OP_ULYSSES_FWD) bytes; holds the
+ *               head-sharded copies of q, k, v, o, lse and the inner plan.
+ * CP_ERR_UNSUPPORTED when cp_size does not divide hq and hkv, or with
+ * interleaved GQA (hq != hkv). */
+cp_status_t cp_ulysses_attn_fwd(const cp_desc_t* desc, const void* q, const void* k, const void* v,
+                                void* o, float* lse,
+                                void* workspace, size_t workspace_bytes, cp_stream_t stream);
+
+/* Ulysses attention backward: the inputs and outputs of cp_attn_bwd, computed
+ * on the head-sharded layout (six re-layouts in, three out).
+ *   workspace : cp_workspace_size(desc, CP_OP_ULYSSES_BWD) bytes. */
+cp_status_t cp_ulysses_attn_bwd(const cp_desc_t* desc, const void* q, const void* k, const void* v,
+                                const void* o, const float* lse, const void* dout,
+                                void* dq, void* dk, void* dv,
+                                void* workspace, size_t workspace_bytes, cp_stream_t stream);
 
 /* Forward without a workspace, for callers that cannot allocate device
  * memory.  The source pages have no counterpart to this entry point.

@@ -20,7 +20,7 @@ cpa = pytest.importorskip("context_long_sequence_zigzag_gb300")
 def _declared_functions():
     src = open(os.path.join(ROOT, "include", "cp_attn.h")).read()
     src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
-    return sorted(set(re.findall(r"\b(cp_[a-z_]+)\s*\(", src)))
+    return sorted(set(re.findall(r"\b(cp_[a-z0-9_]+)\s*\(", src)))
 
 
 def test_library_exports_every_declared_function():
