@@ -24,6 +24,9 @@ Contents and the passage each follows:
   (sequence shards <-> head shards).  "Ulysses Context Parallelism
   的工程取舍全记录" §1.2, §2 (GQA: C divides the KV head count);
   "超长上下文训练速度翻倍秘籍", All2All CP 实现.
+* ``linear_attention`` — decayed linear attention (definition and
+  recurrence) and its AllGather CP state recovery.  "超长上下文训练速度翻倍秘籍",
+  the linear-attention recurrence and the AllGather CP / varlen sections.
 * ``merge``      — the exact log-sum-exp merge of two partial results.
   "Ulysses与Ring-Attention详解" §4.2 (lse_new = log(exp(lse_prev) +
   exp(lse_cur))); "LLM context parallel production guide" "核心原理" (partials
@@ -57,4 +60,10 @@ from .ulysses import (  # noqa: F401
     ulysses_gather,
     ulysses_scatter_lse,
     ulysses_gather_lse,
+)
+from .linear_attention import (  # noqa: F401
+    linear_attn_forward,
+    linear_attn_recurrent,
+    linear_attn_cp,
+    local_state,
 )
