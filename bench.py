@@ -285,6 +285,48 @@ def ulysses_measure(r: Runner, steps: int = 3, warmup: int = 2) -> dict:
             "a2a_q": {"bytes": nbytes, "ms": round(best, 4), "gbs": round(nbytes / (best * 1e-3) / 1e9, 1)}}
 
 
+def linear_measure(dev, steps: int = 5, warmup: int = 3) -> dict:
+    """Decayed linear attention with AllGather CP (cp_lin_attn_fwd) on a
+    long-sequence configuration: S = 64K tokens, 16 heads of 128, C = 8
+    contiguous pieces, bf16, decays alpha = exp(g) in (0.39, 0.95).  The
+    kernels run FP32 FMAs on the CUDA cores: the roofline is the FP32 FMA
+    peak of the unit counts (152 SMs x 128 lanes x 2 FLOP) at the maximum SM
+    clock."""
+    import context_long_sequence_zigzag_gb300 as cpa
+
+    T, H, D, C, B = 65536, 16, 128, 8, 64
+    gen = torch.Generator(device=dev).manual_seed(7)
+    q = (torch.randn(T, H, D, device=dev, generator=gen) * 0.5).to(torch.bfloat16)
+    k = (torch.randn(T, H, D, device=dev, generator=gen) * 0.5).to(torch.bfloat16)
+    v = torch.randn(T, H, D, device=dev, generator=gen).to(torch.bfloat16)
+    g = -torch.rand(H, device=dev, generator=gen) * 0.9 - 0.05
+    prob = cpa.Problem(T, H, H, D, D, C, "contiguous", None, True, D ** -0.5, "blocked", torch.bfloat16)
+    ws = cpa.workspace(prob, cpa.CP_OP_LIN_FWD, dev)
+    o = torch.empty_like(v)
+    times = []
+    for i in range(warmup + steps):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        cpa.cp_lin_attn_fwd(prob, q, k, v, g, o, ws)
+        b.record()
+        if i >= warmup:
+            times.append((a, b))
+    torch.cuda.synchronize()
+    ms = statistics.mean(a.elapsed_time(b) for a, b in times)
+    # chunked form per token and head: local state 2*D*D, intra-chunk scores
+    # and their product with V (B/2 visible keys on average) 2*(B/2)*D each,
+    # initial-state term 2*D*D, state update 2*D*D
+    flops = float(T) * H * (6 * D * D + B * 2 * D)
+    tf = flops / (ms * 1e-3) / 1e12
+    peak = 152 * 128 * 2 * 2.07e9 / 1e12
+    return {"config": {"total_tokens": T, "heads": H, "head_dim": D, "cp_size": C, "layout": "contiguous",
+                       "dtype": "bf16"},
+            "ms": round(ms, 3), "tflops": round(tf, 2),
+            "roofline": {"bound": "alu", "achieved": round(tf, 2), "peak": round(peak, 1), "unit": "TFLOP/s",
+                         "frac": round(tf / peak, 4),
+                         "peak_kind": "FP32 FMA, 152 SMs x 128 lanes x 2 FLOP x 2.07 GHz (unit counts)"}}
+
+
 def e2e_measure(r: Runner, steps: int, warmup: int):
     """Same metric through the ABI with host buffers: pinned host inputs are
     copied in, the step runs, and o, dq, dk, dv are copied back each step."""
@@ -404,6 +446,7 @@ def run_gpu(args):
     e2e_ms, h2d, d2h = e2e_measure(r, max(1, min(args.steps, 3)), 1)
     aux = aux_bandwidth(r)
     uly = ulysses_measure(r) if not args.no_ulysses else {"skipped": "--no-ulysses"}
+    lin = linear_measure(dev) if not args.no_linear else {"skipped": "--no-linear"}
 
     peaks, peak_kind = load_peaks()
     peak_sus = float(peaks.get("bf16_tflops_sustained", FALLBACK["bf16_tflops_sustained"]))
@@ -466,6 +509,7 @@ def run_gpu(args):
             "rank_block_counts": cpa.cp_rank_block_counts(r.prob),
             "rank_balance": balance_report(cpa, w),
             "ulysses": uly,
+            "linear_attention_cp": lin,
         }
         if "ms_per_step" in uly:
             hbm = float(peaks.get("hbm_gbs", FALLBACK["hbm_gbs"]))
@@ -533,6 +577,7 @@ def main():
     ap.add_argument("--cpu-tokens", type=int, default=8192)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-ulysses", action="store_true", help="skip the Ulysses comparison")
+    ap.add_argument("--no-linear", action="store_true", help="skip the linear-attention CP measurement")
     ap.add_argument("--layout", default=None, choices=["contiguous", "zigzag", "striped"],
                     help="shard layout instead of the workload's own (zigzag for the standard ones)")
     args = ap.parse_args()

@@ -40,14 +40,14 @@ CP_LAYOUT_CONTIGUOUS, CP_LAYOUT_ZIGZAG, CP_LAYOUT_STRIPED = 0, 1, 2
 CP_DT_F32, CP_DT_BF16 = 0, 1
 CP_GQA_BLOCKED, CP_GQA_INTERLEAVED = 0, 1
 CP_OP_FWD, CP_OP_BWD, CP_OP_BLOCK_FWD, CP_OP_PERMUTE, CP_OP_BWD_DKDV, CP_OP_BWD_DQ = 0, 1, 2, 3, 4, 5
-CP_OP_ULYSSES_A2A, CP_OP_ULYSSES_FWD, CP_OP_ULYSSES_BWD = 6, 7, 8
+CP_OP_ULYSSES_A2A, CP_OP_ULYSSES_FWD, CP_OP_ULYSSES_BWD, CP_OP_LIN_FWD = 6, 7, 8, 9
 
 EXPORTED = [
     "cp_status_string", "cp_validate", "cp_workspace_size", "cp_shard_offsets",
     "cp_rank_block_counts", "cp_shard_permute", "cp_attn_block_fwd", "cp_lse_merge",
     "cp_attn_fwd", "cp_attn_bwd", "cp_device_status", "cp_check_bounded_wait",
     "cp_attn_fwd_noalloc", "cp_attn_bwd_prep", "cp_attn_bwd_dkdv", "cp_attn_bwd_dq",
-    "cp_ulysses_a2a", "cp_ulysses_attn_fwd", "cp_ulysses_attn_bwd",
+    "cp_ulysses_a2a", "cp_ulysses_attn_fwd", "cp_ulysses_attn_bwd", "cp_lin_attn_fwd",
 ]
 
 
@@ -92,6 +92,7 @@ _sigs = {
     "cp_ulysses_a2a": (ctypes.c_int, [_DP, _P, _P, ctypes.c_int32, ctypes.c_int64, ctypes.c_int32, _P,
                                       ctypes.c_size_t, _P]),
     "cp_ulysses_attn_fwd": (ctypes.c_int, [_DP, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
+    "cp_lin_attn_fwd": (ctypes.c_int, [_DP, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
     "cp_ulysses_attn_bwd": (ctypes.c_int, [_DP, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
 }
 for _name, (_res, _args) in _sigs.items():
@@ -320,6 +321,18 @@ def cp_ulysses_attn_bwd(prob: Problem, q, k, v, o, lse, dout, dq=None, dk=None, 
     _check(_lib.cp_ulysses_attn_bwd(prob.ptr, _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout), _ptr(dq),
                                     _ptr(dk), _ptr(dv), _ptr(ws), ws.numel(), _stream(stream)), "cp_ulysses_attn_bwd")
     return dq, dk, dv
+
+
+def cp_lin_attn_fwd(prob: Problem, q, k, v, g, o=None, ws=None, stream=None):
+    """Decayed linear attention with AllGather CP (contiguous pieces).
+    g: float32 [hq] on the device, log of the per-head decay."""
+    if o is None:
+        o = torch.empty(q.shape[0], q.shape[1], v.shape[2], dtype=q.dtype, device=q.device)
+    if ws is None:
+        ws = workspace(prob, CP_OP_LIN_FWD, q.device)
+    _check(_lib.cp_lin_attn_fwd(prob.ptr, _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(o), _ptr(ws), ws.numel(),
+                                _stream(stream)), "cp_lin_attn_fwd")
+    return o
 
 
 def cp_attn_bwd_prep(prob: Problem, o, dout, dpsum=None, stream=None):

@@ -30,6 +30,7 @@ SOURCES = [
     "device_status.cu",
     "attn_fwd_sm103.cu",
     "attn_bwd_sm103.cu",
+    "linear_attn.cu",
 ]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",

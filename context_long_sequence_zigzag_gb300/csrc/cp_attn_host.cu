@@ -356,6 +356,35 @@ struct BwdLayout {
   size_t fwd_plan, bwd_plan, dpsum, total;
 };
 
+// ---------------------------------------------------------------- linear attention
+// Decayed linear attention has a query head per key/value head (no GQA), a
+// causal recurrence, head dims up to 128, and the AllGather CP of the pages
+// cuts every sequence into C contiguous pieces.
+cp_status_t check_lin(const cp_desc_t* d) {
+  cp_status_t st = check_map_fields(d);
+  if (st != CP_OK) return st;
+  if (d->hq < 1 || d->hkv != d->hq || d->d_qk < 1 || d->d_v < 1) return CP_ERR_INVALID_ARG;
+  if (d->dtype != CP_DT_F32 && d->dtype != CP_DT_BF16) return CP_ERR_INVALID_ARG;
+  if (!(d->scale > 0.f) || !std::isfinite(d->scale)) return CP_ERR_INVALID_ARG;
+  if (d->causal != 1 || d->layout != CP_LAYOUT_CONTIGUOUS) return CP_ERR_UNSUPPORTED;
+  if (d->d_qk > 128 || d->d_v > 128) return CP_ERR_UNSUPPORTED;
+  return CP_OK;
+}
+
+struct LinLayout {
+  size_t pieces, states, init, total;
+};
+LinLayout lin_layout(const cp_desc_t* d) {
+  const size_t np = size_t(d->cp_size) * d->num_seqs;
+  const size_t st = np * d->hq * size_t(d->d_qk) * d->d_v * 4;
+  LinLayout L{};
+  L.pieces = 0;
+  L.states = align256(np * sizeof(LinPiece));
+  L.init = L.states + align256(st);
+  L.total = L.init + align256(st);
+  return L;
+}
+
 // ---------------------------------------------------------------- Ulysses
 // "Ulysses Context Parallelism 的工程取舍全记录" §1.2 / §2: the all-to-all hands
 // rank r heads r*H/C .. (r+1)*H/C - 1 of the whole sequence; with GQA every
@@ -500,6 +529,12 @@ cp_status_t cp_validate(const cp_desc_t* d) { return check_attn_fields(d); }
 
 cp_status_t cp_workspace_size(const cp_desc_t* d, int32_t op, size_t* bytes) {
   if (bytes == nullptr) return CP_ERR_INVALID_ARG;
+  if (op == CP_OP_LIN_FWD) {
+    cp_status_t st = check_lin(d);
+    if (st != CP_OK) return st;
+    *bytes = lin_layout(d).total;
+    return CP_OK;
+  }
   if (op == CP_OP_ULYSSES_A2A) {
     cp_status_t st = check_map_fields(d);
     if (st != CP_OK) return st;
@@ -888,6 +923,31 @@ cp_status_t cp_ulysses_attn_bwd(const cp_desc_t* d, const void* q, const void* k
       launch_ulysses_a2a(perm, T, C, cv, base + L.dv, dv, 1, cs) != cudaSuccess)
     return CP_ERR_CUDA;
   return CP_OK;
+}
+
+cp_status_t cp_lin_attn_fwd(const cp_desc_t* d, const void* q, const void* k, const void* v, const float* g, void* o,
+                            void* ws, size_t ws_bytes, cp_stream_t stream) {
+  cp_status_t st = check_lin(d);
+  if (st != CP_OK) return st;
+  if (d->total_tokens == 0) return CP_OK;
+  const void* ptrs[] = {q, k, v, g, o};
+  for (const void* p : ptrs)
+    if (p == nullptr || !aligned16(p)) return CP_ERR_INVALID_ARG;
+  const LinLayout L = lin_layout(d);
+  if (ws == nullptr || (reinterpret_cast<uintptr_t>(ws) & 255) || ws_bytes < L.total) return CP_ERR_WORKSPACE;
+  const ShardMap m = build_map(d);  // contiguous: piece (r, s) at index r * S + s
+  std::vector<LinPiece> pieces(m.chunks.size());
+  for (size_t i = 0; i < m.chunks.size(); ++i) pieces[i] = LinPiece{int32_t(m.chunks[i].srow0), m.chunks[i].len};
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  char* base = static_cast<char*>(ws);
+  if (cudaMemcpyAsync(base + L.pieces, pieces.data(), pieces.size() * sizeof(LinPiece), cudaMemcpyHostToDevice, cs) !=
+      cudaSuccess)
+    return CP_ERR_CUDA;
+  return launch_lin_attn(reinterpret_cast<const LinPiece*>(base + L.pieces), int32_t(pieces.size()), m.S, m.C, d->hq,
+                         d->d_qk, d->d_v, d->scale, d->dtype, q, k, v, g, reinterpret_cast<float*>(base + L.states),
+                         reinterpret_cast<float*>(base + L.init), o, cs) == cudaSuccess
+             ? CP_OK
+             : CP_ERR_CUDA;
 }
 
 cp_status_t cp_device_status(cp_stream_t stream, int32_t* code) {

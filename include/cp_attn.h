@@ -89,7 +89,7 @@ typedef enum { CP_DT_F32 = 0, CP_DT_BF16 = 1 } cp_dtype_t;
 typedef enum { CP_GQA_BLOCKED = 0, CP_GQA_INTERLEAVED = 1 } cp_gqa_t;
 typedef enum {
   CP_OP_FWD = 0, CP_OP_BWD = 1, CP_OP_BLOCK_FWD = 2, CP_OP_PERMUTE = 3, CP_OP_BWD_DKDV = 4, CP_OP_BWD_DQ = 5,
-  CP_OP_ULYSSES_A2A = 6, CP_OP_ULYSSES_FWD = 7, CP_OP_ULYSSES_BWD = 8
+  CP_OP_ULYSSES_A2A = 6, CP_OP_ULYSSES_FWD = 7, CP_OP_ULYSSES_BWD = 8, CP_OP_LIN_FWD = 9
 } cp_op_t;
 
 /* Problem descriptor.  Read on the host during each call; not retained. */
@@ -242,6 +242,29 @@ cp_status_t cp_ulysses_attn_bwd(const cp_desc_t* desc, const void* q, const void
                                 const void* o, const float* lse, const void* dout,
                                 void* dq, void* dk, void* dv,
                                 void* workspace, size_t workspace_bytes, cp_stream_t stream);
+
+/* ------------------------------------------------------ linear attention
+ * Decayed linear attention with AllGather context parallelism
+ * ("超长上下文训练速度翻倍秘籍": per head h_t = alpha h_{t-1} + k_t^T v_t and
+ * o_t = scale q_t h_t inside each sequence, alpha = exp(g[head]); AllGather
+ * CP: every rank computes the hidden state of its piece from a zero start,
+ * the gathered states give each rank its initial state through the prefix
+ * kv_state = kv_state * alpha^len + cur over the preceding ranks, and the
+ * rank's output is its local output plus (q * alpha^(j+1)) @ init_state for
+ * its j-th token).  The output equals the unsharded recurrence.
+ *   desc      : hq == hkv heads, d_qk (keys/queries) and d_v up to 128,
+ *               causal == 1, layout CONTIGUOUS (pieces cut at floor(r*L/C)),
+ *               dtype bf16 or fp32; scale multiplies q
+ *   q, k      : device [T, hq, d_qk], v / o: device [T, hq, d_v], sharded order
+ *   g         : device float32 [hq], the log of the per-head decay alpha
+ *   workspace : cp_workspace_size(desc, CP_OP_LIN_FWD) bytes: the pieces and
+ *               the gathered ([C * num_seqs, hq, d_qk, d_v] fp32) local and
+ *               recovered initial states
+ * Arithmetic is FP32 on the CUDA cores.  CP_ERR_UNSUPPORTED for another
+ * layout, non-causal or head dims above 128. */
+cp_status_t cp_lin_attn_fwd(const cp_desc_t* desc, const void* q, const void* k, const void* v,
+                            const float* g, void* o,
+                            void* workspace, size_t workspace_bytes, cp_stream_t stream);
 
 /* Forward without a workspace, for callers that cannot allocate device
  * memory.  The source pages have no counterpart to this entry point.

@@ -171,4 +171,14 @@ def test_workspace_sizes_positive_and_ordered():
     assert f > 0 and b > f
     assert cpa.cp_workspace_size(p, cpa.CP_OP_PERMUTE) >= 32
     with pytest.raises(cpa.CpError):
-        cpa.cp_workspace_size(p, 9)
+        cpa.cp_workspace_size(p, 99)  # no such operation
+
+
+def test_linear_attention_rejected_configurations():
+    # AllGather CP of the pages: contiguous pieces, one query head per KV head
+    with pytest.raises(cpa.CpError) as e:
+        cpa.cp_workspace_size(cpa.Problem(256, 2, 2, 64, 64, 2, "zigzag"), cpa.CP_OP_LIN_FWD)
+    assert e.value.status == cpa.CP_ERR_UNSUPPORTED
+    with pytest.raises(cpa.CpError) as e:
+        cpa.cp_workspace_size(cpa.Problem(256, 4, 2, 64, 64, 2, "contiguous"), cpa.CP_OP_LIN_FWD)
+    assert e.value.status == cpa.CP_ERR_INVALID_ARG
