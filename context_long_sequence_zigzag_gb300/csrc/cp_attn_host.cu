@@ -367,19 +367,40 @@ cp_status_t check_lin(const cp_desc_t* d) {
   if (d->dtype != CP_DT_F32 && d->dtype != CP_DT_BF16) return CP_ERR_INVALID_ARG;
   if (!(d->scale > 0.f) || !std::isfinite(d->scale)) return CP_ERR_INVALID_ARG;
   if (d->causal != 1 || d->layout != CP_LAYOUT_CONTIGUOUS) return CP_ERR_UNSUPPORTED;
-  if (d->d_qk > 128 || d->d_v > 128) return CP_ERR_UNSUPPORTED;
+  if (d->d_qk > 128 || d->d_v > 128 || d->d_qk % 8 || d->d_v % 8) return CP_ERR_UNSUPPORTED;
   return CP_OK;
 }
 
-struct LinLayout {
-  size_t pieces, states, init, total;
+// Blocks of every sequence in order: its rank pieces in rank order, each cut
+// into blocks of at most kLinBlock tokens; seq_begin[s] is the first block of
+// sequence s (S + 1 entries).
+struct LinBlocks {
+  std::vector<LinBlock> blocks;
+  std::vector<int32_t> seq_begin;
 };
-LinLayout lin_layout(const cp_desc_t* d) {
-  const size_t np = size_t(d->cp_size) * d->num_seqs;
-  const size_t st = np * d->hq * size_t(d->d_qk) * d->d_v * 4;
+LinBlocks lin_blocks(const ShardMap& m) {
+  LinBlocks B;
+  for (int s = 0; s < m.S; ++s) {
+    B.seq_begin.push_back(int32_t(B.blocks.size()));
+    for (int r = 0; r < m.C; ++r) {
+      const Chunk& c = m.at(r, s, 0);
+      for (int32_t o = 0; o < c.len; o += kLinBlock)
+        B.blocks.push_back(LinBlock{int32_t(c.srow0 + o), std::min(kLinBlock, c.len - o)});
+    }
+  }
+  B.seq_begin.push_back(int32_t(B.blocks.size()));
+  return B;
+}
+
+struct LinLayout {
+  size_t blocks, seq_begin, states, init, total;
+};
+LinLayout lin_layout(const cp_desc_t* d, const LinBlocks& B) {
+  const size_t st = B.blocks.size() * d->hq * size_t(d->d_qk) * d->d_v * 4;
   LinLayout L{};
-  L.pieces = 0;
-  L.states = align256(np * sizeof(LinPiece));
+  L.blocks = 0;
+  L.seq_begin = align256(std::max<size_t>(B.blocks.size(), 1) * sizeof(LinBlock));
+  L.states = L.seq_begin + align256(B.seq_begin.size() * 4);
   L.init = L.states + align256(st);
   L.total = L.init + align256(st);
   return L;
@@ -532,7 +553,7 @@ cp_status_t cp_workspace_size(const cp_desc_t* d, int32_t op, size_t* bytes) {
   if (op == CP_OP_LIN_FWD) {
     cp_status_t st = check_lin(d);
     if (st != CP_OK) return st;
-    *bytes = lin_layout(d).total;
+    *bytes = lin_layout(d, lin_blocks(build_map(d))).total;
     return CP_OK;
   }
   if (op == CP_OP_ULYSSES_A2A) {
@@ -933,18 +954,21 @@ cp_status_t cp_lin_attn_fwd(const cp_desc_t* d, const void* q, const void* k, co
   const void* ptrs[] = {q, k, v, g, o};
   for (const void* p : ptrs)
     if (p == nullptr || !aligned16(p)) return CP_ERR_INVALID_ARG;
-  const LinLayout L = lin_layout(d);
+  const ShardMap m = build_map(d);
+  const LinBlocks B = lin_blocks(m);
+  const LinLayout L = lin_layout(d, B);
   if (ws == nullptr || (reinterpret_cast<uintptr_t>(ws) & 255) || ws_bytes < L.total) return CP_ERR_WORKSPACE;
-  const ShardMap m = build_map(d);  // contiguous: piece (r, s) at index r * S + s
-  std::vector<LinPiece> pieces(m.chunks.size());
-  for (size_t i = 0; i < m.chunks.size(); ++i) pieces[i] = LinPiece{int32_t(m.chunks[i].srow0), m.chunks[i].len};
+  if (B.blocks.empty()) return CP_OK;
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
   char* base = static_cast<char*>(ws);
-  if (cudaMemcpyAsync(base + L.pieces, pieces.data(), pieces.size() * sizeof(LinPiece), cudaMemcpyHostToDevice, cs) !=
-      cudaSuccess)
+  if (cudaMemcpyAsync(base + L.blocks, B.blocks.data(), B.blocks.size() * sizeof(LinBlock), cudaMemcpyHostToDevice,
+                      cs) != cudaSuccess ||
+      cudaMemcpyAsync(base + L.seq_begin, B.seq_begin.data(), B.seq_begin.size() * 4, cudaMemcpyHostToDevice, cs) !=
+          cudaSuccess)
     return CP_ERR_CUDA;
-  return launch_lin_attn(reinterpret_cast<const LinPiece*>(base + L.pieces), int32_t(pieces.size()), m.S, m.C, d->hq,
-                         d->d_qk, d->d_v, d->scale, d->dtype, q, k, v, g, reinterpret_cast<float*>(base + L.states),
+  return launch_lin_attn(reinterpret_cast<const LinBlock*>(base + L.blocks), int32_t(B.blocks.size()),
+                         reinterpret_cast<const int32_t*>(base + L.seq_begin), m.S, d->hq, d->d_qk, d->d_v, d->scale,
+                         d->dtype, q, k, v, g, reinterpret_cast<float*>(base + L.states),
                          reinterpret_cast<float*>(base + L.init), o, cs) == cudaSuccess
              ? CP_OK
              : CP_ERR_CUDA;

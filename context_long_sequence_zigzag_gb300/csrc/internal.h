@@ -89,16 +89,18 @@ enum : int32_t {
 // ---- launchers (each returns cudaSuccess or the launch error) ----
 cudaError_t launch_permute(const CopySeg* segs, int32_t nseg, int64_t npieces,
                            const void* in, void* out, cudaStream_t st);
-// Linear attention with AllGather CP: one contiguous piece of one sequence
-// held by one rank (rank-major order: piece (r, s) = r * S + s).
-struct LinPiece {
+// Linear attention with AllGather CP: a block of at most kLinBlock tokens of
+// one rank's piece of one sequence; blocks are listed per sequence in order
+// (ranks in order, blocks in order inside a rank).
+constexpr int32_t kLinBlock = 512;
+struct LinBlock {
   int32_t row0;  // first sharded row
   int32_t len;   // tokens
 };
 size_t lin_output_smem(int32_t Dk, int32_t Dv);
-cudaError_t launch_lin_attn(const LinPiece* pieces, int32_t npieces, int32_t S, int32_t C, int32_t H, int32_t Dk,
-                            int32_t Dv, float scale, int32_t dtype, const void* q, const void* k, const void* v,
-                            const float* g, float* states, float* init, void* o, cudaStream_t st);
+cudaError_t launch_lin_attn(const LinBlock* blocks, int32_t nblocks, const int32_t* seq_begin, int32_t S, int32_t H,
+                            int32_t Dk, int32_t Dv, float scale, int32_t dtype, const void* q, const void* k,
+                            const void* v, const float* g, float* states, float* init, void* o, cudaStream_t st);
 
 // Ulysses re-layout: perm[s] = global row of sharded row s (T entries, device).
 cudaError_t launch_ulysses_a2a(const int32_t* perm, int64_t T, int32_t C, int64_t chunk_bytes, const void* in,

@@ -7,16 +7,20 @@
 // made a vectorised prefix and a fused correction instead of per-rank and
 // per-sub-sequence loops).
 //
-// With alpha = exp(g) per head, three kernels:
-//   lin_state_kernel  — per (piece, head): S = sum_s alpha^(n-1-s) k_s^T v_s,
-//                        the hidden state at the piece end from a zero start
-//                        (one decay-weighted K^T V product);
-//   lin_prefix_kernel — per (sequence, head): init_0 = 0,
-//                        init_{r+1} = alpha^(n_r) init_r + S_r;
-//   lin_output_kernel — per (piece, head): chunked decayed attention of the
-//                        piece started from init_r, which equals the local
-//                        output plus the page's correction, in one pass.
-// FP32 CUDA-core arithmetic (head dims up to 128); bf16 or fp32 in and out.
+// With alpha = exp(g) per head, every rank piece is cut into blocks of at most
+// kLinBlock tokens (the unit of parallel work), and three kernels run:
+//   lin_state_kernel  — per (block, head): S = sum_s alpha^(n-1-s) k_s^T v_s,
+//                        the hidden state at the block end from a zero start;
+//   lin_prefix_kernel — per (sequence, head): the decayed prefix over the
+//                        gathered states in sequence order (ranks in order,
+//                        blocks in order inside a rank): init_b = cur,
+//                        cur = alpha^(n_b) cur + S_b; at rank granularity this
+//                        is the page's state recovery;
+//   lin_output_kernel — per (block, head): chunked decayed attention of the
+//                        block started from init_b, i.e. the local output plus
+//                        the page's correction, in one pass.
+// FP32 CUDA-core arithmetic, register-tiled (head dims multiples of 8, up to
+// 128); bf16 or fp32 tensors.
 #include <cuda_bf16.h>
 
 #include "internal.h"
@@ -25,8 +29,8 @@ namespace cpattn {
 namespace {
 
 constexpr int kLinB = 64;      // tokens per chunk
-constexpr int kLinMaxD = 128;  // head dims up to 128
 constexpr int kLinThreads = 256;
+constexpr int kLdPad = 1;      // Q/K rows padded to an odd stride (bank spread)
 
 __device__ __forceinline__ float to_f(float x) { return x; }
 __device__ __forceinline__ float to_f(__nv_bfloat16 x) { return __bfloat162float(x); }
@@ -38,7 +42,7 @@ template <>
 __device__ __forceinline__ __nv_bfloat16 from_f<__nv_bfloat16>(float x) { return __float2bfloat16_rn(x); }
 
 // Rows [row0, row0 + n) of a [T, H, D] tensor, head h, into smem rows of
-// `ld` floats (ld >= D) as fp32, each row multiplied by w(row), zero past n.
+// `ld` floats as fp32, each row times w(row); zeros past n.
 template <typename T, typename W>
 __device__ __forceinline__ void load_rows(float* dst, int ld, const T* src, int64_t row0, int n, int H, int h, int D,
                                           W w) {
@@ -48,172 +52,227 @@ __device__ __forceinline__ void load_rows(float* dst, int ld, const T* src, int6
   }
 }
 
+// acc[8][8] += sum_s (w_s K[s][d_i]) V[s][j_jj], thread tile rows ty*8.., cols tx*8..
+__device__ __forceinline__ void kv_outer(float (&acc)[8][8], const float* Ks, int ldk, const float* Vs, int ldv,
+                                         const float* Ws, int n, int ty, int tx, int Dk, int Dv) {
+  const int d0 = ty * 8, j0 = tx * 8;
+  if (d0 >= Dk || j0 >= Dv) return;
+  for (int s = 0; s < n; ++s) {
+    const float w = Ws ? Ws[s] : 1.f;
+    float kr[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) kr[i] = Ks[s * ldk + d0 + i] * w;
+    const float4 v0 = *reinterpret_cast<const float4*>(Vs + s * ldv + j0);
+    const float4 v1 = *reinterpret_cast<const float4*>(Vs + s * ldv + j0 + 4);
+    const float vr[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+#pragma unroll
+      for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(kr[i], vr[j], acc[i][j]);
+  }
+}
+
 template <typename T>
-__global__ void __launch_bounds__(kLinThreads) lin_state_kernel(const LinPiece* __restrict__ pieces, int32_t H,
+__global__ void __launch_bounds__(kLinThreads) lin_state_kernel(const LinBlock* __restrict__ blocks, int32_t H,
                                                                  int32_t Dk, int32_t Dv, const T* __restrict__ k,
                                                                  const T* __restrict__ v, const float* __restrict__ g,
                                                                  float* __restrict__ states) {
-  extern __shared__ float lsm[];
-  float* Ks = lsm;                  // [kLinB][Dk]
-  float* Vs = lsm + kLinB * Dk;     // [kLinB][Dv]
-  const int p = blockIdx.x / H, h = blockIdx.x - (blockIdx.x / H) * H;
-  const LinPiece pc = pieces[p];
+  extern __shared__ __align__(16) float lsm[];
+  const int ldk = Dk + kLdPad;
+  float* Ks = lsm;                 // [kLinB][Dk + 1]
+  float* Vs = Ks + kLinB * ldk;    // [kLinB][Dv]  (offset rounded to 4 floats below)
+  Vs = reinterpret_cast<float*>((reinterpret_cast<uintptr_t>(Vs) + 15) & ~uintptr_t(15));
+  const int b = blockIdx.x / H, h = blockIdx.x - (blockIdx.x / H) * H;
+  const LinBlock bl = blocks[b];
   const float gh = g[h];
-  // thread (ty, tx) owns S rows ty*8.. and columns tx*8..
   const int ty = threadIdx.x / 16, tx = threadIdx.x % 16;
   float acc[8][8] = {};
-  for (int c0 = 0; c0 < pc.len; c0 += kLinB) {
-    const int n = min(kLinB, pc.len - c0);
-    const int last = pc.len - 1 - c0;  // exponent of row 0 of this chunk
-    load_rows(Ks, Dk, k, pc.row0 + c0, n, H, h, Dk, [&](int t) { return __expf(gh * float(last - t)); });
-    load_rows(Vs, Dv, v, pc.row0 + c0, n, H, h, Dv, [](int) { return 1.f; });
+  for (int c0 = 0; c0 < bl.len; c0 += kLinB) {
+    const int n = min(kLinB, bl.len - c0);
+    const int last = bl.len - 1 - c0;  // exponent of chunk row 0
     __syncthreads();
-    for (int s = 0; s < n; ++s) {
-      float kr[8], vr[8];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        kr[i] = (ty * 8 + i < Dk) ? Ks[s * Dk + ty * 8 + i] : 0.f;
-        vr[i] = (tx * 8 + i < Dv) ? Vs[s * Dv + tx * 8 + i] : 0.f;
-      }
-#pragma unroll
-      for (int i = 0; i < 8; ++i)
-#pragma unroll
-        for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(kr[i], vr[j], acc[i][j]);
-    }
+    load_rows(Ks, ldk, k, bl.row0 + c0, n, H, h, Dk, [&](int t) { return __expf(gh * float(last - t)); });
+    load_rows(Vs, Dv, v, bl.row0 + c0, n, H, h, Dv, [](int) { return 1.f; });
     __syncthreads();
+    kv_outer(acc, Ks, ldk, Vs, Dv, nullptr, n, ty, tx, Dk, Dv);
   }
-  float* out = states + (int64_t(p) * H + h) * Dk * Dv;
+  float* out = states + (int64_t(b) * H + h) * Dk * Dv;
+  if (ty * 8 < Dk && tx * 8 < Dv)
 #pragma unroll
-  for (int i = 0; i < 8; ++i)
+    for (int i = 0; i < 8; ++i)
 #pragma unroll
-    for (int j = 0; j < 8; ++j)
-      if (ty * 8 + i < Dk && tx * 8 + j < Dv) out[(ty * 8 + i) * Dv + tx * 8 + j] = acc[i][j];
+      for (int j = 0; j < 8; ++j) out[(ty * 8 + i) * Dv + tx * 8 + j] = acc[i][j];
 }
 
-// pieces are rank-major: piece (r, s) = r * S + s
-__global__ void __launch_bounds__(kLinThreads) lin_prefix_kernel(const LinPiece* __restrict__ pieces, int32_t S,
-                                                                  int32_t C, int32_t H, int32_t DD,
-                                                                  const float* __restrict__ g,
+// per (sequence, head): blocks of sequence s in order are [seq_begin[s], seq_begin[s+1])
+__global__ void __launch_bounds__(kLinThreads) lin_prefix_kernel(const LinBlock* __restrict__ blocks,
+                                                                  const int32_t* __restrict__ seq_begin, int32_t H,
+                                                                  int32_t DD, const float* __restrict__ g,
                                                                   const float* __restrict__ states,
                                                                   float* __restrict__ init) {
   const int s = blockIdx.x / H, h = blockIdx.x - (blockIdx.x / H) * H;
   const float gh = g[h];
+  const int b0 = seq_begin[s], b1 = seq_begin[s + 1];
   for (int e = threadIdx.x; e < DD; e += blockDim.x) {
     float cur = 0.f;
-    for (int r = 0; r < C; ++r) {
-      const int64_t p = int64_t(r) * S + s;
-      const int64_t idx = (p * H + h) * DD + e;
+    for (int b = b0; b < b1; ++b) {
+      const int64_t idx = (int64_t(b) * H + h) * DD + e;
       init[idx] = cur;
-      cur = __expf(gh * float(pieces[p].len)) * cur + states[idx];
+      cur = __expf(gh * float(blocks[b].len)) * cur + states[idx];
     }
   }
 }
 
 template <typename T>
-__global__ void __launch_bounds__(kLinThreads) lin_output_kernel(const LinPiece* __restrict__ pieces, int32_t H,
+__global__ void __launch_bounds__(kLinThreads) lin_output_kernel(const LinBlock* __restrict__ blocks, int32_t H,
                                                                   int32_t Dk, int32_t Dv, float scale,
                                                                   const T* __restrict__ q, const T* __restrict__ k,
                                                                   const T* __restrict__ v, const float* __restrict__ g,
                                                                   const float* __restrict__ init, T* __restrict__ o) {
-  extern __shared__ float lsm[];
-  const int ldk = Dk + 1;              // padded K rows: lanes walking s hit distinct banks
+  extern __shared__ __align__(16) float lsm[];
+  const int ldq = Dk + 4;              // 16-byte rows, rows ty*4 and ty*4+4 on different banks
+  const int ldk = Dk + kLdPad;
+  constexpr int lda = kLinB + 4;
   float* Hs = lsm;                     // [Dk][Dv] carried state
-  float* Qs = Hs + Dk * Dv;            // [kLinB][Dk]
-  float* Ks = Qs + kLinB * Dk;         // [kLinB][Dk + 1]
-  float* Vs = Ks + kLinB * ldk;        // [kLinB][Dv]
-  float* As = Vs + kLinB * Dv;         // [kLinB][kLinB] decayed causal scores
-  float* Ws = As + kLinB * kLinB;      // [kLinB] alpha^(n-1-s) of the state update
-  float* Ds = Ws + kLinB;              // [kLinB] alpha^(t+1) of the initial-state term
-  const int p = blockIdx.x / H, h = blockIdx.x - (blockIdx.x / H) * H;
-  const LinPiece pc = pieces[p];
+  float* Vs = Hs + Dk * Dv;            // [kLinB][Dv]
+  float* Qs = Vs + kLinB * Dv;         // [kLinB][Dk + 4]
+  float* As = Qs + kLinB * ldq;        // [kLinB][kLinB + 4], A transposed: As[s][t]
+  float* Ws = As + kLinB * lda;        // [kLinB] alpha^(n-1-s)
+  float* Ds = Ws + kLinB;              // [kLinB] alpha^(t+1)
+  float* Ks = Ds + kLinB;              // [kLinB][Dk + 1]
+  const int b = blockIdx.x / H, h = blockIdx.x - (blockIdx.x / H) * H;
+  const LinBlock bl = blocks[b];
   const float gh = g[h];
   const int DD = Dk * Dv;
-  const float* h0 = init + (int64_t(p) * H + h) * DD;
+  const float* h0 = init + (int64_t(b) * H + h) * DD;
   for (int e = threadIdx.x; e < DD; e += blockDim.x) Hs[e] = h0[e];
-  for (int c0 = 0; c0 < pc.len; c0 += kLinB) {
-    const int n = min(kLinB, pc.len - c0);
-    __syncthreads();  // previous chunk's readers of Qs/Ks/Vs/As and writers of Hs are done
-    load_rows(Qs, Dk, q, pc.row0 + c0, n, H, h, Dk, [](int) { return 1.f; });
-    load_rows(Ks, ldk, k, pc.row0 + c0, n, H, h, Dk, [](int) { return 1.f; });
-    load_rows(Vs, Dv, v, pc.row0 + c0, n, H, h, Dv, [](int) { return 1.f; });
+  const int ty = threadIdx.x / 16, tx = threadIdx.x % 16;
+  for (int c0 = 0; c0 < bl.len; c0 += kLinB) {
+    const int n = min(kLinB, bl.len - c0);
+    __syncthreads();  // the previous chunk is finished with every buffer
+    load_rows(Qs, ldq, q, bl.row0 + c0, n, H, h, Dk, [](int) { return 1.f; });
+    load_rows(Ks, ldk, k, bl.row0 + c0, n, H, h, Dk, [](int) { return 1.f; });
+    load_rows(Vs, Dv, v, bl.row0 + c0, n, H, h, Dv, [](int) { return 1.f; });
     for (int t = threadIdx.x; t < kLinB; t += blockDim.x) {
       Ws[t] = t < n ? __expf(gh * float(n - 1 - t)) : 0.f;
       Ds[t] = __expf(gh * float(t + 1));
     }
     __syncthreads();
-    // A[t][s] = (q_t . k_s) alpha^(t-s) for s <= t
-    for (int e = threadIdx.x; e < kLinB * kLinB; e += blockDim.x) {
-      const int t = e / kLinB, s = e - t * kLinB;
-      float a = 0.f;
-      if (s <= t && t < n) {
-        for (int d = 0; d < Dk; ++d) a = fmaf(Qs[t * Dk + d], Ks[s * ldk + d], a);
-        a *= __expf(gh * float(t - s));
+    // ---- A[t][s] = (q_t . k_s) alpha^(t-s), s <= t (4x4 tile: t = ty*4+i, s = tx*4+j)
+    {
+      float a[4][4] = {};
+      for (int d = 0; d < Dk; ++d) {
+        float qv[4], kv[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          qv[i] = Qs[(ty * 4 + i) * ldq + d];
+          kv[i] = Ks[(tx * 4 + i) * ldk + d];
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+          for (int j = 0; j < 4; ++j) a[i][j] = fmaf(qv[i], kv[j], a[i][j]);
       }
-      As[e] = a;
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int t = ty * 4 + i, s = tx * 4 + j;
+          As[s * lda + t] = (s <= t) ? a[i][j] * __expf(gh * float(t - s)) : 0.f;
+        }
     }
     __syncthreads();
-    // O[t][j] = scale (sum_s A[t][s] V[s][j] + alpha^(t+1) sum_d Q[t][d] H[d][j])
-    for (int e = threadIdx.x; e < kLinB * Dv; e += blockDim.x) {
-      const int t = e / Dv, j = e - t * Dv;
-      if (t >= n) continue;
-      float x = 0.f, y = 0.f;
-      for (int s = 0; s <= t; ++s) x = fmaf(As[t * kLinB + s], Vs[s * Dv + j], x);
-      for (int d = 0; d < Dk; ++d) y = fmaf(Qs[t * Dk + d], Hs[d * Dv + j], y);
-      o[((pc.row0 + c0 + t) * int64_t(H) + h) * Dv + j] = from_f<T>(scale * (x + Ds[t] * y));
+    // ---- O[t][j] = scale (sum_s A[t][s] V[s][j] + alpha^(t+1) sum_d Q[t][d] H[d][j])
+    //      (4x8 tile: t = ty*4+i, j = tx*8+jj)
+    if (tx * 8 < Dv) {
+      const int j0 = tx * 8;
+      float x[4][8] = {}, y[4][8] = {};
+      for (int s = 0; s < kLinB; ++s) {
+        const float4 av = *reinterpret_cast<const float4*>(As + s * lda + ty * 4);
+        const float ar[4] = {av.x, av.y, av.z, av.w};
+        const float4 v0 = *reinterpret_cast<const float4*>(Vs + s * Dv + j0);
+        const float4 v1 = *reinterpret_cast<const float4*>(Vs + s * Dv + j0 + 4);
+        const float vr[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+          for (int jj = 0; jj < 8; ++jj) x[i][jj] = fmaf(ar[i], vr[jj], x[i][jj]);
+      }
+      for (int d = 0; d < Dk; ++d) {
+        float qr[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) qr[i] = Qs[(ty * 4 + i) * ldq + d];
+        const float4 h0v = *reinterpret_cast<const float4*>(Hs + d * Dv + j0);
+        const float4 h1v = *reinterpret_cast<const float4*>(Hs + d * Dv + j0 + 4);
+        const float hr[8] = {h0v.x, h0v.y, h0v.z, h0v.w, h1v.x, h1v.y, h1v.z, h1v.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+          for (int jj = 0; jj < 8; ++jj) y[i][jj] = fmaf(qr[i], hr[jj], y[i][jj]);
+      }
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int t = ty * 4 + i;
+        if (t < n) {
+          T* dst = o + ((bl.row0 + c0 + t) * int64_t(H) + h) * Dv + j0;
+#pragma unroll
+          for (int jj = 0; jj < 8; ++jj) dst[jj] = from_f<T>(scale * (x[i][jj] + Ds[t] * y[i][jj]));
+        }
+      }
     }
-    __syncthreads();
-    // H = alpha^n H + sum_s alpha^(n-1-s) k_s^T v_s
-    const float an = __expf(gh * float(n));
-    for (int e = threadIdx.x; e < DD; e += blockDim.x) {
-      const int d = e / Dv, j = e - d * Dv;
-      float x = 0.f;
-      for (int s = 0; s < n; ++s) x = fmaf(Ws[s] * Ks[s * ldk + d], Vs[s * Dv + j], x);
-      Hs[e] = an * Hs[e] + x;
+    __syncthreads();  // every thread read Hs before it is updated
+    // ---- H = alpha^n H + sum_s alpha^(n-1-s) k_s^T v_s (8x8 tile: d = ty*8+i, j = tx*8+jj)
+    {
+      float acc[8][8] = {};
+      kv_outer(acc, Ks, ldk, Vs, Dv, Ws, n, ty, tx, Dk, Dv);
+      const float an = __expf(gh * float(n));
+      if (ty * 8 < Dk && tx * 8 < Dv)
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+#pragma unroll
+          for (int jj = 0; jj < 8; ++jj) {
+            float* p = Hs + (ty * 8 + i) * Dv + tx * 8 + jj;
+            *p = an * *p + acc[i][jj];
+          }
     }
   }
+}
+
+size_t state_smem(int32_t Dk, int32_t Dv) {
+  return sizeof(float) * (size_t(kLinB) * (Dk + kLdPad) + 4 + size_t(kLinB) * Dv);
 }
 
 }  // namespace
 
 size_t lin_output_smem(int32_t Dk, int32_t Dv) {
-  return sizeof(float) * (size_t(Dk) * Dv + kLinB * Dk + kLinB * (Dk + 1) + kLinB * Dv + kLinB * kLinB + 2 * kLinB);
+  return sizeof(float) * (size_t(Dk) * Dv + size_t(kLinB) * Dv + size_t(kLinB) * (Dk + 4) +
+                          size_t(kLinB) * (kLinB + 4) + 2 * kLinB + size_t(kLinB) * (Dk + kLdPad));
 }
 
-cudaError_t launch_lin_attn(const LinPiece* pieces, int32_t npieces, int32_t S, int32_t C, int32_t H, int32_t Dk,
-                            int32_t Dv, float scale, int32_t dtype, const void* q, const void* k, const void* v,
-                            const float* g, float* states, float* init, void* o, cudaStream_t st) {
-  if (Dk > kLinMaxD || Dv > kLinMaxD) return cudaErrorInvalidValue;
-  const unsigned grid = unsigned(int64_t(npieces) * H);
+cudaError_t launch_lin_attn(const LinBlock* blocks, int32_t nblocks, const int32_t* seq_begin, int32_t S, int32_t H,
+                            int32_t Dk, int32_t Dv, float scale, int32_t dtype, const void* q, const void* k,
+                            const void* v, const float* g, float* states, float* init, void* o, cudaStream_t st) {
+  if (Dk > 128 || Dv > 128 || Dk % 8 || Dv % 8) return cudaErrorInvalidValue;
+  const unsigned grid = unsigned(int64_t(nblocks) * H);
   if (grid == 0) return cudaSuccess;
-  const size_t sm_state = sizeof(float) * size_t(kLinB) * (Dk + Dv);
-  const size_t sm_out = lin_output_smem(Dk, Dv);
-  cudaError_t e;
-  if (dtype == CP_DT_BF16) {
-    auto ks = lin_state_kernel<__nv_bfloat16>;
-    auto ko = lin_output_kernel<__nv_bfloat16>;
+  const size_t sm_state = state_smem(Dk, Dv), sm_out = lin_output_smem(Dk, Dv);
+  auto run = [&](auto ks, auto ko, auto tag) -> cudaError_t {
+    using E = decltype(tag);
+    cudaError_t e;
     if ((e = cudaFuncSetAttribute(ks, cudaFuncAttributeMaxDynamicSharedMemorySize, int(sm_state))) != cudaSuccess ||
         (e = cudaFuncSetAttribute(ko, cudaFuncAttributeMaxDynamicSharedMemorySize, int(sm_out))) != cudaSuccess)
       return e;
-    ks<<<grid, kLinThreads, sm_state, st>>>(pieces, H, Dk, Dv, static_cast<const __nv_bfloat16*>(k),
-                                            static_cast<const __nv_bfloat16*>(v), g, states);
-    lin_prefix_kernel<<<unsigned(S * H), kLinThreads, 0, st>>>(pieces, S, C, H, Dk * Dv, g, states, init);
-    ko<<<grid, kLinThreads, sm_out, st>>>(pieces, H, Dk, Dv, scale, static_cast<const __nv_bfloat16*>(q),
-                                          static_cast<const __nv_bfloat16*>(k), static_cast<const __nv_bfloat16*>(v),
-                                          g, init, static_cast<__nv_bfloat16*>(o));
-  } else {
-    auto ks = lin_state_kernel<float>;
-    auto ko = lin_output_kernel<float>;
-    if ((e = cudaFuncSetAttribute(ks, cudaFuncAttributeMaxDynamicSharedMemorySize, int(sm_state))) != cudaSuccess ||
-        (e = cudaFuncSetAttribute(ko, cudaFuncAttributeMaxDynamicSharedMemorySize, int(sm_out))) != cudaSuccess)
-      return e;
-    ks<<<grid, kLinThreads, sm_state, st>>>(pieces, H, Dk, Dv, static_cast<const float*>(k),
-                                            static_cast<const float*>(v), g, states);
-    lin_prefix_kernel<<<unsigned(S * H), kLinThreads, 0, st>>>(pieces, S, C, H, Dk * Dv, g, states, init);
-    ko<<<grid, kLinThreads, sm_out, st>>>(pieces, H, Dk, Dv, scale, static_cast<const float*>(q),
-                                          static_cast<const float*>(k), static_cast<const float*>(v), g, init,
-                                          static_cast<float*>(o));
-  }
-  return cudaGetLastError();
+    ks<<<grid, kLinThreads, sm_state, st>>>(blocks, H, Dk, Dv, static_cast<const E*>(k), static_cast<const E*>(v), g,
+                                            states);
+    lin_prefix_kernel<<<unsigned(S * H), kLinThreads, 0, st>>>(blocks, seq_begin, H, Dk * Dv, g, states, init);
+    ko<<<grid, kLinThreads, sm_out, st>>>(blocks, H, Dk, Dv, scale, static_cast<const E*>(q),
+                                          static_cast<const E*>(k), static_cast<const E*>(v), g, init,
+                                          static_cast<E*>(o));
+    return cudaGetLastError();
+  };
+  if (dtype == CP_DT_BF16)
+    return run(lin_state_kernel<__nv_bfloat16>, lin_output_kernel<__nv_bfloat16>, __nv_bfloat16{});
+  return run(lin_state_kernel<float>, lin_output_kernel<float>, float{});
 }
 
 }  // namespace cpattn

@@ -257,11 +257,14 @@ cp_status_t cp_ulysses_attn_bwd(const cp_desc_t* desc, const void* q, const void
  *               dtype bf16 or fp32; scale multiplies q
  *   q, k      : device [T, hq, d_qk], v / o: device [T, hq, d_v], sharded order
  *   g         : device float32 [hq], the log of the per-head decay alpha
- *   workspace : cp_workspace_size(desc, CP_OP_LIN_FWD) bytes: the pieces and
- *               the gathered ([C * num_seqs, hq, d_qk, d_v] fp32) local and
- *               recovered initial states
+ *   workspace : cp_workspace_size(desc, CP_OP_LIN_FWD) bytes: the block list
+ *               and the gathered local and recovered initial states (fp32
+ *               [blocks, hq, d_qk, d_v]; every rank piece is cut into blocks of
+ *               at most 512 tokens, the unit of parallel work, and the prefix
+ *               runs over the blocks of a sequence in order — ranks in order,
+ *               blocks in order inside a rank)
  * Arithmetic is FP32 on the CUDA cores.  CP_ERR_UNSUPPORTED for another
- * layout, non-causal or head dims above 128. */
+ * layout, non-causal, or head dims above 128 or not multiples of 8. */
 cp_status_t cp_lin_attn_fwd(const cp_desc_t* desc, const void* q, const void* k, const void* v,
                             const float* g, void* o,
                             void* workspace, size_t workspace_bytes, cp_stream_t stream);
