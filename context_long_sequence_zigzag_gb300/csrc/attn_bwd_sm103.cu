@@ -209,7 +209,10 @@ __device__ __forceinline__ float load_stat(const AttnArgs& a, const StepCursor<B
 template <int DQK, int BNQ>
 struct DkdvCfg {
   static constexpr int kKPanels = DQK / 64;
-  static constexpr int NS = DQK == 128 ? 2 : 3;  // stages of (Q, dO)
+  // Q(i) is read by S(i) and, a full step later, by dK(i); dO(i) by dP(i) and
+  // dV(i) within the step: Q gets the deeper ring.
+  static constexpr int NSQ = DQK == 128 ? 3 : 4;  // stages of Q
+  static constexpr int NSO = DQK == 128 ? 2 : 3;  // stages of dO
   static constexpr uint32_t kQPanel = BNQ * 128;  // BNQ rows x 64 bf16 columns
   static constexpr uint32_t kKBytes = kKPanels * kPanel;
   static constexpr uint32_t kVBytes = 2 * kPanel;
@@ -217,11 +220,11 @@ struct DkdvCfg {
   static constexpr uint32_t kOBytes = 2 * kQPanel;
   static constexpr uint32_t offK = 0;
   static constexpr uint32_t offV = offK + kKBytes;
-  static constexpr uint32_t offQ = offV + kVBytes;       // NS stages
-  static constexpr uint32_t offO = offQ + NS * kQBytes;  // NS stages
-  static constexpr uint32_t offStat = offO + NS * kOBytes;  // [2][2*BNQ] floats
+  static constexpr uint32_t offQ = offV + kVBytes;        // NSQ stages
+  static constexpr uint32_t offO = offQ + NSQ * kQBytes;  // NSO stages
+  static constexpr uint32_t offStat = offO + NSO * kOBytes;  // [2][2*BNQ] floats
   static constexpr uint32_t offBar = offStat + 2 * 2 * BNQ * 4;
-  static constexpr int kNumBars = 1 + 3 * NS + 9;
+  static constexpr int kNumBars = 1 + 2 * NSQ + 2 * NSO + 9;
   static constexpr uint32_t kSmem = offBar + kNumBars * 8 + 16;
   // TMEM columns
   static constexpr uint32_t tS = 0, tDP = BNQ, tDV = 2 * BNQ, tDK = 2 * BNQ + DV;
@@ -251,10 +254,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dkdv_kernel(const __grid
 
   const uint32_t bar0 = sbase + Cfg::offBar;
   const uint32_t bar_kv = bar0;
-  auto bar_q_full = [&](int s) { return bar0 + 8u * (1 + s); };                  // Q of stage s landed
-  auto bar_q_empty = [&](int s) { return bar0 + 8u * (1 + Cfg::NS + s); };
-  auto bar_o_full = [&](int s) { return bar0 + 8u * (1 + 2 * Cfg::NS + s); };   // dO of stage s landed
-  const uint32_t bar_s_full = bar0 + 8u * (1 + 3 * Cfg::NS);
+  auto bar_q_full = [&](int s) { return bar0 + 8u * (1 + s); };                    // Q of stage s landed
+  auto bar_q_empty = [&](int s) { return bar0 + 8u * (1 + Cfg::NSQ + s); };        // dK read it
+  auto bar_o_full = [&](int s) { return bar0 + 8u * (1 + 2 * Cfg::NSQ + s); };     // dO of stage s landed
+  auto bar_o_empty = [&](int s) { return bar0 + 8u * (1 + 2 * Cfg::NSQ + Cfg::NSO + s); };  // dV read it
+  const uint32_t bar_s_full = bar0 + 8u * (1 + 2 * Cfg::NSQ + 2 * Cfg::NSO);
   const uint32_t bar_dp_full = bar_s_full + 8;
   const uint32_t bar_p_full = bar_s_full + 16;
   const uint32_t bar_ds_full = bar_s_full + 24;
@@ -267,10 +271,13 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dkdv_kernel(const __grid
 
   if (threadIdx.x == 0) {
     ptx::mbar_init(bar_kv, 1);
-    for (int s = 0; s < Cfg::NS; ++s) {
+    for (int s = 0; s < Cfg::NSQ; ++s) {
       ptx::mbar_init(bar_q_full(s), 1);
       ptx::mbar_init(bar_q_empty(s), 1);
+    }
+    for (int s = 0; s < Cfg::NSO; ++s) {
       ptx::mbar_init(bar_o_full(s), 1);
+      ptx::mbar_init(bar_o_empty(s), 1);
     }
     ptx::mbar_init(bar_s_full, 1);
     ptx::mbar_init(bar_dp_full, 1);
@@ -313,13 +320,15 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dkdv_kernel(const __grid
         for (int c = 0; c < 2; ++c)
           ptx::tma_load_3d(sbase + Cfg::offV + c * kPanel, &p.tv, bar_kv, c * 64, kvh, tile.row0);
       }
+      const int NS = qstream ? Cfg::NSQ : Cfg::NSO;
       auto full = [&](int st) { return qstream ? bar_q_full(st) : bar_o_full(st); };
+      auto empty = [&](int st) { return qstream ? bar_q_empty(st) : bar_o_empty(st); };
       StepCursor<BNQ> cur;
       cur.init(a.ranges, tile.range_begin, tile.range_count, G, kvh, a.hkv, a.gqa_interleaved);
       for (int i = 0; i < n_steps; ++i, cur.next()) {
-        const int st = i % Cfg::NS;
-        // stage st is free once dK of its previous occupant (the last reader of Q and dO) completed
-        if (i >= Cfg::NS && !ptx::mbar_wait(bar_q_empty(st), ((i / Cfg::NS) - 1) & 1, kSiteQEmpty, wctx)) break;
+        const int st = i % NS;
+        // stage st is free once the last reader of its previous occupant completed
+        if (i >= NS && !ptx::mbar_wait(empty(st), ((i / NS) - 1) & 1, kSiteQEmpty, wctx)) break;
         const int h = cur.head();
         if (qstream) {
           ptx::mbar_arrive_expect_tx(full(st), Cfg::kQBytes);
@@ -338,8 +347,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dkdv_kernel(const __grid
         volatile int no_abort = 0;
         const ptx::WaitCtx drain{&no_abort, nullptr, kWaitLimitNs};
         if (qstream) ptx::mbar_wait(bar_kv, 0, kSiteDrain, drain);
-        for (int i = max(0, issued - Cfg::NS); i < issued; ++i)
-          ptx::mbar_wait(full(i % Cfg::NS), (i / Cfg::NS) & 1, kSiteDrain, drain);
+        for (int i = max(0, issued - NS); i < issued; ++i) ptx::mbar_wait(full(i % NS), (i / NS) & 1, kSiteDrain, drain);
       }
     }
   } else if (warp == 9) {
@@ -350,8 +358,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dkdv_kernel(const __grid
       constexpr uint32_t idDK = ptx::idesc_bf16_f32(BT, DQK, false, true);  // B = Q, MN-major
       const uint32_t tS = tmem + Cfg::tS, tDP = tmem + Cfg::tDP, tDV = tmem + Cfg::tDV, tDK = tmem + Cfg::tDK;
       const uint32_t kb = sbase + Cfg::offK, vb = sbase + Cfg::offV;
-      auto qb = [&](int i) { return sbase + Cfg::offQ + (i % Cfg::NS) * Cfg::kQBytes; };
-      auto ob = [&](int i) { return sbase + Cfg::offO + (i % Cfg::NS) * Cfg::kOBytes; };
+      auto qb = [&](int i) { return sbase + Cfg::offQ + (i % Cfg::NSQ) * Cfg::kQBytes; };
+      auto ob = [&](int i) { return sbase + Cfg::offO + (i % Cfg::NSO) * Cfg::kOBytes; };
       // D = A (K-major panels of 128 rows) x B^T (K-major panels of BNQ rows)
       auto issue_ss = [&](uint32_t d, uint32_t abase, uint32_t bbase, int ksteps) {
         const uint64_t da = ptx::sdesc_sw128(abase, 16, 1024), db = ptx::sdesc_sw128(bbase, 16, 1024);
@@ -381,9 +389,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dkdv_kernel(const __grid
           if (!ptx::mbar_wait_w(bar_ds_full, (i - 1) & 1, kSiteDSFull, wctx)) { ok = false; break; }
           ptx::tc_fence_after();
           issue_ts(tDK, tDP, qb(i - 1), idDK, i - 1 > 0);
-          ptx::mma_commit_w(bar_q_empty((i - 1) % Cfg::NS));
+          ptx::mma_commit_w(bar_q_empty((i - 1) % Cfg::NSQ));
         }
-        if (!ptx::mbar_wait_w(bar_o_full(i % Cfg::NS), (i / Cfg::NS) & 1, kSiteQFull, wctx)) { ok = false; break; }
+        if (!ptx::mbar_wait_w(bar_o_full(i % Cfg::NSO), (i / Cfg::NSO) & 1, kSiteQFull, wctx)) { ok = false; break; }
         ptx::tc_fence_after();
         issue_ss(tDP, vb, ob(i), DV / 16);
         ptx::mma_commit_w(bar_dp_full);
@@ -391,8 +399,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dkdv_kernel(const __grid
         if (!ptx::mbar_wait_w(bar_p_full, i & 1, kSitePFull, wctx)) { ok = false; break; }
         ptx::tc_fence_after();
         issue_ts(tDV, tS, ob(i), idDV, i > 0);
+        ptx::mma_commit_w(bar_o_empty(i % Cfg::NSO));
         if (i + 1 < n_steps) {
-          if (!ptx::mbar_wait_w(bar_q_full((i + 1) % Cfg::NS), ((i + 1) / Cfg::NS) & 1, kSiteQFull, wctx)) {
+          if (!ptx::mbar_wait_w(bar_q_full((i + 1) % Cfg::NSQ), ((i + 1) / Cfg::NSQ) & 1, kSiteQFull, wctx)) {
             ok = false;
             break;
           }
