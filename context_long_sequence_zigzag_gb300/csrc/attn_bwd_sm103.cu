@@ -196,14 +196,41 @@ __device__ __forceinline__ int count_steps(const RangeDesc* ranges, int begin, i
   return n;
 }
 
-// Statistic of query column t (0..BNQ-1: lse * log2e; BNQ..2BNQ-1: D * scale)
-// of the step the cursor points at.
+// Negated statistic of query column t (0..BNQ-1: -lse * log2e;
+// BNQ..2BNQ-1: -D * scale) of the step the cursor points at.  Stored negated
+// so that a pair of them is directly the addend of a packed FMA.
 template <int BNQ>
 __device__ __forceinline__ float load_stat(const AttnArgs& a, const StepCursor<BNQ>& c, int t) {
   const int col = t % BNQ;
   if (t >= 2 * BNQ || col >= c.n()) return 0.f;
   const int64_t idx = int64_t(c.head()) * a.T + c.row() + col;
-  return t < BNQ ? a.lse_in[idx] * kLog2e : a.dpsum[idx] * a.scale;
+  return t < BNQ ? -(a.lse_in[idx] * kLog2e) : -(a.dpsum[idx] * a.scale);
+}
+
+// v[0..3] = exp2(s[c0..c0+3] * sl2 + nl[0..3]) with two packed FMAs
+template <int NC>
+__device__ __forceinline__ void exp4(const uint32_t (&x)[NC / 32][32], int c0, uint64_t sl2x2, const float4 nl,
+                                     float* v) {
+  const uint64_t y0 = ptx::fma_f32x2(ptx::f32x2(colv<NC>(x, c0), colv<NC>(x, c0 + 1)), sl2x2, ptx::f32x2(nl.x, nl.y));
+  const uint64_t y1 =
+      ptx::fma_f32x2(ptx::f32x2(colv<NC>(x, c0 + 2), colv<NC>(x, c0 + 3)), sl2x2, ptx::f32x2(nl.z, nl.w));
+  float t[4];
+  ptx::f32x2_split(y0, t[0], t[1]);
+  ptx::f32x2_split(y1, t[2], t[3]);
+#pragma unroll
+  for (int e = 0; e < 4; ++e) v[e] = ptx::ex2(t[e]);
+}
+
+// v[0..3] *= s[c0..c0+3] * scale + nd[0..3] with packed FMAs and products
+template <int NC>
+__device__ __forceinline__ void ds4(const uint32_t (&x)[NC / 32][32], int c0, uint64_t scx2, const float4 nd,
+                                    float* v) {
+  const uint64_t y0 = ptx::fma_f32x2(ptx::f32x2(colv<NC>(x, c0), colv<NC>(x, c0 + 1)), scx2, ptx::f32x2(nd.x, nd.y));
+  const uint64_t y1 = ptx::fma_f32x2(ptx::f32x2(colv<NC>(x, c0 + 2), colv<NC>(x, c0 + 3)), scx2, ptx::f32x2(nd.z, nd.w));
+  const uint64_t p0 = ptx::mul_f32x2(ptx::f32x2(v[0], v[1]), y0);
+  const uint64_t p1 = ptx::mul_f32x2(ptx::f32x2(v[2], v[3]), y1);
+  ptx::f32x2_split(p0, v[0], v[1]);
+  ptx::f32x2_split(p1, v[2], v[3]);
 }
 
 template <int DQK, int BNQ>
@@ -435,6 +462,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dkdv_kernel(const __grid
     const uint32_t colS = grp * NC;
     const uint32_t colPk = grp ? Cfg::kPk1 : 0;
     const float sl2 = a.scale * kLog2e;
+    const uint64_t sl2x2 = ptx::f32x2(sl2, sl2), scx2 = ptx::f32x2(a.scale, a.scale);
     const int kpos = tile.pos0 + r;
     const int nk = tile.nrows;
     bool ok = true;
@@ -473,23 +501,13 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dkdv_kernel(const __grid
       if (need_mask) {
 #pragma unroll
         for (int j = 0; j < NC; j += 4) {
-          const float4 l4 = *reinterpret_cast<const float4*>(sL + colS + j);
-          const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+          exp4<NC>(x, j, sl2x2, *reinterpret_cast<const float4*>(sL + colS + j), pf + j);
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int c = j + e;
-            const float pv = ptx::ex2(fmaf(colv<NC>(x, c), sl2, -lv[e]));
-            pf[c] = (c >= cmin && c < cmax) ? pv : 0.f;
-          }
+          for (int e = 0; e < 4; ++e) pf[j + e] = (j + e >= cmin && j + e < cmax) ? pf[j + e] : 0.f;
         }
       } else {
 #pragma unroll
-        for (int j = 0; j < NC; j += 4) {
-          const float4 l4 = *reinterpret_cast<const float4*>(sL + colS + j);
-          const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
-#pragma unroll
-          for (int e = 0; e < 4; ++e) pf[j + e] = ptx::ex2(fmaf(colv<NC>(x, j + e), sl2, -lv[e]));
-        }
+        for (int j = 0; j < NC; j += 4) exp4<NC>(x, j, sl2x2, *reinterpret_cast<const float4*>(sL + colS + j), pf + j);
       }
       st_bf16<NC>(tS + colPk, pf);
       ptx::tmem_st_wait();
@@ -502,12 +520,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dkdv_kernel(const __grid
       ptx::tc_fence_after();
       ldcols<NC>(tDP + colS, x);
 #pragma unroll
-      for (int j = 0; j < NC; j += 4) {
-        const float4 d4 = *reinterpret_cast<const float4*>(sD + colS + j);
-        const float dv4[4] = {d4.x, d4.y, d4.z, d4.w};
-#pragma unroll
-        for (int e = 0; e < 4; ++e) pf[j + e] *= fmaf(colv<NC>(x, j + e), a.scale, -dv4[e]);
-      }
+      for (int j = 0; j < NC; j += 4) ds4<NC>(x, j, scx2, *reinterpret_cast<const float4*>(sD + colS + j), pf + j);
       st_bf16<NC>(tDP + colPk, pf);
       ptx::tmem_st_wait();
       ptx::tc_fence_before();
@@ -823,6 +836,7 @@ __global__ void __launch_bounds__(kThreadsDq, 1) attn_bwd_dq_kernel(const __grid
     const uint32_t tS = tmem + lane_base + Cfg::tS, tDP = tmem + lane_base + Cfg::tDP;
     const uint32_t colS = grp * 64;
     const float sl2 = a.scale * kLog2e;
+    const uint64_t sl2x2 = ptx::f32x2(sl2, sl2), scx2 = ptx::f32x2(a.scale, a.scale);
     const bool row_ok = r < tile.nrows;
     const int qpos = tile.pos0 + r;
     const int64_t qrow = int64_t(tile.row0) + r;
@@ -869,15 +883,17 @@ __global__ void __launch_bounds__(kThreadsDq, 1) attn_bwd_dq_kernel(const __grid
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(bar_p_full);  // S(j) has been read
       float pf[64];
+      const float4 nl4 = make_float4(-lse2, -lse2, -lse2, -lse2);
       if (need_mask) {  // warp-uniform: diagonal and ragged tiles only
 #pragma unroll
-        for (int c = 0; c < 64; ++c) {
-          const float pv = ptx::ex2(fmaf(colv<64>(x, c), sl2, -lse2));
-          pf[c] = c < lim ? pv : 0.f;
+        for (int c = 0; c < 64; c += 4) {
+          exp4<64>(x, c, sl2x2, nl4, pf + c);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) pf[c + e] = c + e < lim ? pf[c + e] : 0.f;
         }
       } else {
 #pragma unroll
-        for (int c = 0; c < 64; ++c) pf[c] = ptx::ex2(fmaf(colv<64>(x, c), sl2, -lse2));
+        for (int c = 0; c < 64; c += 4) exp4<64>(x, c, sl2x2, nl4, pf + c);
       }
       // ---- dS = P (dP - D) * scale
       if (!__all_sync(0xffffffffu, ptx::mbar_wait(bar_dp_full, j & 1, kSiteDPFull, wctx))) { ok = false; break; }
@@ -886,8 +902,9 @@ __global__ void __launch_bounds__(kThreadsDq, 1) attn_bwd_dq_kernel(const __grid
       ptx::tc_fence_before();
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(bar_dp_read);  // dP(j) has been read
+      const float4 nd4 = make_float4(-dsc, -dsc, -dsc, -dsc);
 #pragma unroll
-      for (int c = 0; c < 64; ++c) pf[c] *= fmaf(colv<64>(x, c), a.scale, -dsc);
+      for (int c = 0; c < 64; c += 4) ds4<64>(x, c, scx2, nd4, pf + c);
       // dS buffer j % NB was last read by dQ(j - NB)
       if (j >= NB && !__all_sync(0xffffffffu, ptx::mbar_wait(bar_dq_done(j % NB), ((j - NB) / NB) & 1,
                                                              kSiteDSFull, wctx))) {

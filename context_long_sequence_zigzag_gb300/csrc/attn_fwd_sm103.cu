@@ -11,25 +11,30 @@
 // maximum and the running row sum rescale the TMEM output accumulator, so
 // the result equals merging every block's partial exactly.
 //
-// Both products read their A operand from TMEM (one issuing thread reaches
-// noticeably more tensor throughput with TS than with SS MMAs at N = 128):
-//   Q  (bf16, two per column) is written into TMEM once by the softmax
-//      threads, so S = Q K^T is a TS MMA with K streamed through shared memory;
-//   P  (bf16) overwrites the first half of its S buffer, so O += P V is a TS
-//      MMA with V read from shared memory as an MN-major operand.
-// TMEM columns: Q [0, DQK/2), S0 and S1 (128 each, double-buffered so S of
-// the next key tile is computed while the softmax works on this one), O
-// (DV).  MMA order S(0), S(1), PV(0), S(2), PV(1), S(3), ...
+// S = Q K^T is an SS MMA (Q, loaded once, and the streamed K both K-major in
+// shared memory) into one of three TMEM S buffers; P (bf16) overwrites the
+// first half of its S buffer, so O += P V is a TS MMA with V read from shared
+// memory as an MN-major operand.  TMEM columns: S0, S1, S2 (128 each), O (DV)
+// = 512.  S(j+3) reuses buffer j % 3 once PV(j) has completed.  With three
+// buffers the S of the next two key tiles is already computed while the
+// softmax works on this one, so the softmax never waits for the PV -> S round
+// trip of the step before.
 //
-// Roles (192 threads):
-//   warps 0-3  softmax: thread t owns query row t = TMEM lane t.  Writes its
-//              Q row into TMEM, then per key tile loads S, masks, takes the
-//              row maximum, exponentiates, writes P back to TMEM, rescales O
-//              when the reference maximum moves by more than 2^8, and finally
-//              normalises O and writes o / lse.
-//   warp 4     TMA producers: lane 0 streams K, lane 1 streams V, each into
-//              its own ring.
-//   warp 5     TMEM allocator and MMA issuer.
+// Two warps issue the MMAs, one the S products and one the PV products.
+// The tensor pipe queues only about two and a half MMAs, so every cycle an
+// issuing warp spends on its commits, barrier waits and loop overhead idles
+// the pipe unless another warp is issuing meanwhile.
+//
+// Roles (224 threads):
+//   warps 0-3  softmax: thread t owns query row t = TMEM lane t.  Per key
+//              tile it loads S, masks, takes the row maximum, exponentiates,
+//              writes P back to TMEM, rescales O when the reference maximum
+//              moves by more than 2^8, and finally normalises O and writes
+//              o / lse.
+//   warp 4     TMA producers: lane 0 loads Q, then streams K; lane 1 streams
+//              V, each into its own ring.
+//   warp 5     TMEM allocator; issues S(j) = Q K(j)^T.
+//   warp 6     issues O += P(j) V(j).
 #include <cuda.h>
 #include <cuda_bf16.h>
 
@@ -59,24 +64,26 @@ struct FwdCfg {
   static constexpr int kVPanels = DV / 64;
   static constexpr int NSK = DQK <= 128 ? 3 : 2;
   static constexpr int NSV = DQK <= 128 ? 3 : 2;
+  static constexpr int NS_S = 3;  // TMEM S buffers
+  static constexpr uint32_t kQBytes = kQPanels * kSubTile;
   static constexpr uint32_t kKBytes = kQPanels * kSubTile;
   static constexpr uint32_t kVBytes = kVPanels * kSubTile;
-  static constexpr uint32_t offK = 0;
+  static constexpr uint32_t offQ = 0;
+  static constexpr uint32_t offK = offQ + kQBytes;
   static constexpr uint32_t offV = offK + NSK * kKBytes;
   static constexpr uint32_t offBar = offV + NSV * kVBytes;
-  static constexpr int kNumBars = 1 + 2 * NSK + 2 * NSV + 6;
+  static constexpr int kNumBars = 1 + 2 * NSK + 2 * NSV + 3 * NS_S + 2;
   static constexpr uint32_t kSmem = offBar + kNumBars * 8 + 16;
   // TMEM columns
-  static constexpr uint32_t tQ = 0;
-  static constexpr uint32_t tS0 = DQK / 2;
-  static constexpr uint32_t tO = tS0 + 2 * BN;
+  static constexpr uint32_t tS0 = 0;
+  static constexpr uint32_t tO = NS_S * BN;
   static constexpr uint32_t kTmemCols = 512;
   static_assert(tO + DV <= kTmemCols, "TMEM budget");
   static_assert(kSmem <= 232448, "shared memory budget");
 };
 
 struct FwdParams {
-  CUtensorMap tk, tv;
+  CUtensorMap tq, tk, tv;
   AttnArgs a;
   int32_t* err;
 };
@@ -113,7 +120,7 @@ __device__ __forceinline__ int head_of_slot(int slot, const AttnArgs& a) {
 }
 
 template <int DQK, int DV>
-__global__ void __launch_bounds__(192, 1) attn_fwd_tc_kernel(const __grid_constant__ FwdParams p) {
+__global__ void __launch_bounds__(224, 1) attn_fwd_tc_kernel(const __grid_constant__ FwdParams p) {
   using Cfg = FwdCfg<DQK, DV>;
   extern __shared__ __align__(1024) uint8_t smem[];
   const uint32_t sbase = ptx::smem_u32(smem);
@@ -131,21 +138,25 @@ __global__ void __launch_bounds__(192, 1) attn_fwd_tc_kernel(const __grid_consta
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   const uint32_t bar0 = sbase + Cfg::offBar;
-  const uint32_t bar_q = bar0;  // Q is in TMEM (4 softmax warps)
+  const uint32_t bar_q = bar0;  // Q tile landed in shared memory
   auto bar_k_full = [&](int s) { return bar0 + 8u * (1 + s); };
   auto bar_k_empty = [&](int s) { return bar0 + 8u * (1 + Cfg::NSK + s); };
   auto bar_v_full = [&](int s) { return bar0 + 8u * (1 + 2 * Cfg::NSK + s); };
   auto bar_v_empty = [&](int s) { return bar0 + 8u * (1 + 2 * Cfg::NSK + Cfg::NSV + s); };
   const uint32_t barx = bar0 + 8u * (1 + 2 * Cfg::NSK + 2 * Cfg::NSV);
-  auto bar_s_full = [&](int b) { return barx + 8u * b; };  // S buffer b computed
-  const uint32_t bar_p_full = barx + 16;                   // P(j) in TMEM (4 softmax warps)
-  const uint32_t bar_o_done = barx + 24;                   // PV(j) done
-  const uint32_t bar_drain = barx + 32;
+  // One (S computed, P written, PV done) triple per S buffer b = j % 3: the
+  // softmax may run up to two key tiles ahead of the MMA issuer, and a
+  // per-buffer barrier is then never more than one phase ahead of a waiter,
+  // which is what a parity wait needs.
+  auto bar_s_full = [&](int b) { return barx + 8u * b; };
+  auto bar_p_full = [&](int b) { return barx + 8u * (Cfg::NS_S + b); };      // 4 softmax warps
+  auto bar_o_done = [&](int b) { return barx + 8u * (2 * Cfg::NS_S + b); };  // PV(j) done
+  auto bar_drain = [&](int w) { return barx + 8u * (3 * Cfg::NS_S + w); };    // per issuing warp
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Cfg::offBar + Cfg::kNumBars * 8);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Cfg::offBar + Cfg::kNumBars * 8 + 4);
 
   if (threadIdx.x == 0) {
-    ptx::mbar_init(bar_q, 4);
+    ptx::mbar_init(bar_q, 1);
     for (int s = 0; s < Cfg::NSK; ++s) {
       ptx::mbar_init(bar_k_full(s), 1);
       ptx::mbar_init(bar_k_empty(s), 1);
@@ -154,11 +165,13 @@ __global__ void __launch_bounds__(192, 1) attn_fwd_tc_kernel(const __grid_consta
       ptx::mbar_init(bar_v_full(s), 1);
       ptx::mbar_init(bar_v_empty(s), 1);
     }
-    ptx::mbar_init(bar_s_full(0), 1);
-    ptx::mbar_init(bar_s_full(1), 1);
-    ptx::mbar_init(bar_p_full, 4);
-    ptx::mbar_init(bar_o_done, 1);
-    ptx::mbar_init(bar_drain, 1);
+    for (int b = 0; b < Cfg::NS_S; ++b) {
+      ptx::mbar_init(bar_s_full(b), 1);
+      ptx::mbar_init(bar_p_full(b), 4);
+      ptx::mbar_init(bar_o_done(b), 1);
+    }
+    ptx::mbar_init(bar_drain(0), 1);
+    ptx::mbar_init(bar_drain(1), 1);
     *abort_flag = 0;
     ptx::fence_barrier_init();
   }
@@ -167,6 +180,7 @@ __global__ void __launch_bounds__(192, 1) attn_fwd_tc_kernel(const __grid_consta
     ptx::tmem_relinquish();
   }
   if (warp == 4 && lane == 0) {
+    ptx::prefetch_tmap(&p.tq);
     ptx::prefetch_tmap(&p.tk);
     ptx::prefetch_tmap(&p.tv);
   }
@@ -178,8 +192,14 @@ __global__ void __launch_bounds__(192, 1) attn_fwd_tc_kernel(const __grid_consta
 
   if (warp == 4) {
     // ------------------------------------------------------------ producers
-    // Lane 0 streams K, lane 1 streams V: on GB300 one thread's tiled TMA
-    // loads top out near 40 B/cycle, two issuing threads reach about 60.
+    // Lane 0 loads Q, then streams K; lane 1 streams V: on GB300 one
+    // thread's tiled TMA loads top out near 40 B/cycle, two issuing threads
+    // reach about 60.
+    if (lane == 0 && n_kv > 0) {
+      ptx::mbar_arrive_expect_tx(bar_q, Cfg::kQBytes);
+      for (int c = 0; c < Cfg::kQPanels; ++c)
+        ptx::tma_load_3d(sbase + Cfg::offQ + c * kSubTile, &p.tq, bar_q, c * 64, h, tile.row0);
+    }
     if (lane < 2 && n_kv > 0) {
       const bool kstream = lane == 0;
       const int NS = kstream ? Cfg::NSK : Cfg::NSV;
@@ -204,66 +224,62 @@ __global__ void __launch_bounds__(192, 1) attn_fwd_tc_kernel(const __grid_consta
         // Let every copy still in flight land before the CTA exits.
         volatile int no_abort = 0;
         const ptx::WaitCtx drain{&no_abort, nullptr, kWaitLimitNs};
+        if (kstream) ptx::mbar_wait(bar_q, 0, kSiteDrain, drain);
         for (int j = max(0, issued - NS); j < issued; ++j) ptx::mbar_wait(full(j % NS), (j / NS) & 1, kSiteDrain, drain);
       }
     }
-  } else if (warp == 5) {
-    // ------------------------------------------------------------ MMA issuer (whole warp)
+  } else if (warp == 5 || warp == 6) {
+    // ------------------------------------------------------------ MMA issuers (whole warps)
     if (n_kv > 0) {
-      constexpr uint32_t idS = ptx::idesc_bf16_f32(BM, BN, false, false);
-      constexpr uint32_t idO = ptx::idesc_bf16_f32(BM, DV, false, true);
-      const uint32_t tO = tmem + Cfg::tO;
-      // S(j) = Q K(j)^T into S buffer j & 1 (A = Q from TMEM)
-      auto issue_s = [&](int j) {
-        const int sk = j % Cfg::NSK;
-        const uint64_t kd = ptx::sdesc_sw128(sbase + Cfg::offK + sk * Cfg::kKBytes, 16, 1024);
-        const uint32_t tS = tmem + Cfg::tS0 + BN * (j & 1);
-#pragma unroll
-        for (int kk = 0; kk < DQK / 16; ++kk)
-          ptx::mma_ts_w(tS, tmem + Cfg::tQ + kk * 8, kd + (((kk >> 2) * kSubTile + (kk & 3) * 32) >> 4), idS, kk > 0);
-        ptx::mma_commit_w(bar_s_full(j & 1));
-        ptx::mma_commit_w(bar_k_empty(sk));
-      };
-      bool ok = ptx::mbar_wait_w(bar_q, 0, kSiteQ, wctx) && ptx::mbar_wait_w(bar_k_full(0), 0, kSiteKFull, wctx);
-      if (ok) {
-        ptx::tc_fence_after();
-        issue_s(0);
-      }
-      if (ok && n_kv > 1) {
-        ok = ptx::mbar_wait_w(bar_k_full(1 % Cfg::NSK), (1 / Cfg::NSK) & 1, kSiteKFull, wctx);
-        if (ok) {
-          ptx::tc_fence_after();
-          issue_s(1);
-        }
-      }
-      for (int j = 0; ok && j < n_kv; ++j) {
-        const int sv = j % Cfg::NSV;
-        ok = ptx::mbar_wait_w(bar_p_full, j & 1, kSitePFull, wctx) &&
-             ptx::mbar_wait_w(bar_v_full(sv), (j / Cfg::NSV) & 1, kSiteVFull, wctx);
-        if (!ok) break;
-        ptx::tc_fence_after();
-        // O += P(j) V(j), P(j) over the first half of S buffer j & 1
-        const uint64_t vd = ptx::sdesc_sw128(sbase + Cfg::offV + sv * Cfg::kVBytes, kSubTile, 1024);
-        const uint32_t tP = tmem + Cfg::tS0 + BN * (j & 1);
-#pragma unroll
-        for (int kk = 0; kk < BN / 16; ++kk)
-          ptx::mma_ts_w(tO, tP + kk * 8, vd + ((kk * 2048) >> 4), idO, (j > 0 || kk > 0));
-        ptx::mma_commit_w(bar_o_done);
-        ptx::mma_commit_w(bar_v_empty(sv));
-        // S(j+2) reuses buffer j & 1 once PV(j) has been issued
-        if (j + 2 < n_kv) {
-          ok = ptx::mbar_wait_w(bar_k_full((j + 2) % Cfg::NSK), ((j + 2) / Cfg::NSK) & 1, kSiteKFull, wctx);
+      bool ok = true;
+      if (warp == 5) {
+        // S(j) = Q K(j)^T into S buffer j % 3 (A = Q, B = K, both K-major in
+        // shared memory), once PV(j-3) has finished reading that buffer
+        constexpr uint32_t idS = ptx::idesc_bf16_f32(BM, BN, false, false);
+        const uint64_t qd = ptx::sdesc_sw128(sbase + Cfg::offQ, 16, 1024);
+        ok = ptx::mbar_wait_w(bar_q, 0, kSiteQ, wctx);
+        for (int j = 0; ok && j < n_kv; ++j) {
+          const int sk = j % Cfg::NSK, sb = j % Cfg::NS_S;
+          if (j >= Cfg::NS_S)
+            ok = ptx::mbar_wait_w(bar_o_done(sb), ((j - Cfg::NS_S) / Cfg::NS_S) & 1, kSiteOFull, wctx);
+          ok = ok && ptx::mbar_wait_w(bar_k_full(sk), (j / Cfg::NSK) & 1, kSiteKFull, wctx);
           if (!ok) break;
           ptx::tc_fence_after();
-          issue_s(j + 2);
+          const uint64_t kd = ptx::sdesc_sw128(sbase + Cfg::offK + sk * Cfg::kKBytes, 16, 1024);
+          const uint32_t tS = tmem + Cfg::tS0 + BN * sb;
+#pragma unroll
+          for (int kk = 0; kk < DQK / 16; ++kk) {
+            const uint32_t adv = ((kk >> 2) * kSubTile + (kk & 3) * 32) >> 4;
+            ptx::mma_ss_w(tS, qd + adv, kd + adv, idS, kk > 0);
+          }
+          ptx::mma_commit_w(bar_s_full(sb));
+          ptx::mma_commit_w(bar_k_empty(sk));
+        }
+      } else {
+        // O += P(j) V(j), P(j) over the first half of S buffer j % 3
+        constexpr uint32_t idO = ptx::idesc_bf16_f32(BM, DV, false, true);
+        const uint32_t tO = tmem + Cfg::tO;
+        for (int j = 0; ok && j < n_kv; ++j) {
+          const int sv = j % Cfg::NSV, sb = j % Cfg::NS_S;
+          ok = ptx::mbar_wait_w(bar_p_full(sb), (j / Cfg::NS_S) & 1, kSitePFull, wctx) &&
+               ptx::mbar_wait_w(bar_v_full(sv), (j / Cfg::NSV) & 1, kSiteVFull, wctx);
+          if (!ok) break;
+          ptx::tc_fence_after();
+          const uint64_t vd = ptx::sdesc_sw128(sbase + Cfg::offV + sv * Cfg::kVBytes, kSubTile, 1024);
+          const uint32_t tP = tmem + Cfg::tS0 + BN * sb;
+#pragma unroll
+          for (int kk = 0; kk < BN / 16; ++kk)
+            ptx::mma_ts_w(tO, tP + kk * 8, vd + ((kk * 2048) >> 4), idO, (j > 0 || kk > 0));
+          ptx::mma_commit_w(bar_o_done(sb));
+          ptx::mma_commit_w(bar_v_empty(sv));
         }
       }
       if (!ok) {
-        // Wait for every MMA already issued before TMEM is released.
+        // Wait for every MMA this warp already issued before TMEM is released.
         volatile int no_abort = 0;
         const ptx::WaitCtx drain{&no_abort, nullptr, kWaitLimitNs};
-        ptx::mma_commit_w(bar_drain);
-        ptx::mbar_wait_w(bar_drain, 0, kSiteDrain, drain);
+        ptx::mma_commit_w(bar_drain(warp - 5));
+        ptx::mbar_wait_w(bar_drain(warp - 5), 0, kSiteDrain, drain);
       }
     }
   } else {
@@ -275,37 +291,15 @@ __global__ void __launch_bounds__(192, 1) attn_fwd_tc_kernel(const __grid_consta
     const int qpos = tile.pos0 + row;
     const bool row_ok = row < tile.nrows;
     const int64_t qrow = int64_t(tile.row0) + row;
-    // Q row -> TMEM (bf16 pairs are already the A-operand packing)
-    if (n_kv > 0) {
-      const uint4* src = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(a.q) +
-                                                        (qrow * a.hq + h) * DQK);
-      const bool in_range = qrow < a.T;
-#pragma unroll
-      for (int c = 0; c < DQK / 64; ++c) {
-        uint32_t qr[32];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const uint4 v = in_range ? __ldg(src + c * 8 + i) : make_uint4(0, 0, 0, 0);
-          qr[4 * i] = v.x;
-          qr[4 * i + 1] = v.y;
-          qr[4 * i + 2] = v.z;
-          qr[4 * i + 3] = v.w;
-        }
-        ptx::tmem_st32(tmem + lane_base + Cfg::tQ + c * 32, qr);
-      }
-      ptx::tmem_st_wait();
-      ptx::tc_fence_before();
-      __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(bar_q);
-    }
     float m_ref = -INFINITY;  // reference maximum of scale*log2e*s (log2 units)
     float l = 0.f;
     bool ok = true;
     KvCursor cur;
     cur.init(a.ranges, tile.range_begin, tile.range_count);
     for (int j = 0; j < n_kv; ++j, cur.next()) {
-      const uint32_t tS = tmem + lane_base + Cfg::tS0 + BN * (j & 1);
-      if (!__all_sync(0xffffffffu, ptx::mbar_wait(bar_s_full(j & 1), (j >> 1) & 1, kSiteSFull, wctx))) {
+      const int sb = j % Cfg::NS_S;
+      const uint32_t tS = tmem + lane_base + Cfg::tS0 + BN * sb;
+      if (!__all_sync(0xffffffffu, ptx::mbar_wait(bar_s_full(sb), (j / Cfg::NS_S) & 1, kSiteSFull, wctx))) {
         ok = false;
         break;
       }
@@ -350,30 +344,40 @@ __global__ void __launch_bounds__(192, 1) attn_fwd_tc_kernel(const __grid_consta
         m_ref = m_new;
       }
       const float mref = m_ref == -INFINITY ? 0.f : m_ref;
-      float r8[8];
+      // row sum in 8 chains, as 4 packed pairs
+      uint64_t r2[4];
 #pragma unroll
-      for (int e = 0; e < 8; ++e) r8[e] = 0.f;
+      for (int e = 0; e < 4; ++e) r2[e] = 0ull;
+      const uint64_t sl2x2 = ptx::f32x2(sl2, sl2), nmx2 = ptx::f32x2(-mref, -mref);
       // P = exp2(s * scale * log2e - m_ref) (bf16, two per column) over the
-      // first half of the S buffer; PV(j-2) read it before S(j) was issued
+      // first half of the S buffer; PV(j-3) finished reading it before S(j)
+      // was issued
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         uint32_t pk[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
-          const float e0 = ptx::ex2(fmaf(__uint_as_float(sr[c][2 * i]), sl2, -mref));
-          const float e1 = ptx::ex2(fmaf(__uint_as_float(sr[c][2 * i + 1]), sl2, -mref));
-          r8[(2 * i) & 7] += e0;
-          r8[(2 * i + 1) & 7] += e1;
+          const uint64_t x = ptx::fma_f32x2(
+              ptx::f32x2(__uint_as_float(sr[c][2 * i]), __uint_as_float(sr[c][2 * i + 1])), sl2x2, nmx2);
+          float x0, x1;
+          ptx::f32x2_split(x, x0, x1);
+          const float e0 = ptx::ex2(x0), e1 = ptx::ex2(x1);
+          r2[i & 3] = ptx::add_f32x2(r2[i & 3], ptx::f32x2(e0, e1));
           pk[i] = ptx::pack_bf16(e0, e1);
         }
         ptx::tmem_st16(tS + c * 16, pk);
       }
+      float r8[8];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) ptx::f32x2_split(r2[e], r8[2 * e], r8[2 * e + 1]);
       const float rs = ((r8[0] + r8[1]) + (r8[2] + r8[3])) + ((r8[4] + r8[5]) + (r8[6] + r8[7]));
       l = l * alpha + rs;
       // O may be rescaled once PV(j-1) is complete (rare: the reference
       // maximum only moves when a row's maximum grows by more than 2^8)
       if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
-        if (!__all_sync(0xffffffffu, ptx::mbar_wait(bar_o_done, (j - 1) & 1, kSiteOFull, wctx))) {
+        const int jp = j - 1;  // PV(j-1) done implies every earlier PV is (in-order pipe)
+        if (!__all_sync(0xffffffffu, ptx::mbar_wait(bar_o_done(jp % Cfg::NS_S), (jp / Cfg::NS_S) & 1, kSiteOFull,
+                                                     wctx))) {
           ok = false;
           break;
         }
@@ -392,11 +396,14 @@ __global__ void __launch_bounds__(192, 1) attn_fwd_tc_kernel(const __grid_consta
       ptx::tmem_st_wait();
       ptx::tc_fence_before();
       __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(bar_p_full);
+      if (lane == 0) ptx::mbar_arrive(bar_p_full(sb));
     }
 
     // ------------------------------------------------------------ epilogue
-    if (ok && n_kv > 0) ok = __all_sync(0xffffffffu, ptx::mbar_wait(bar_o_done, (n_kv - 1) & 1, kSiteOFull, wctx));
+    if (ok && n_kv > 0) {
+      const int jl = n_kv - 1;
+      ok = __all_sync(0xffffffffu, ptx::mbar_wait(bar_o_done(jl % Cfg::NS_S), (jl / Cfg::NS_S) & 1, kSiteOFull, wctx));
+    }
     if (ok) {
       ptx::tc_fence_after();
       const float inv = l > 0.f ? 1.f / l : 0.f;
@@ -486,7 +493,9 @@ static cudaError_t launch_fwd_impl(const AttnArgs& a, cudaStream_t st) {
   FwdParams p;
   p.a = a;
   p.err = device_error_word();
-  if (!make_map_3d(&p.tk, a.k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, DQK, a.hkv, a.T, 64, BN,
+  if (!make_map_3d(&p.tq, a.q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, DQK, a.hq, a.T, 64, BM,
+                   CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !make_map_3d(&p.tk, a.k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, DQK, a.hkv, a.T, 64, BN,
                    CU_TENSOR_MAP_SWIZZLE_128B) ||
       !make_map_3d(&p.tv, a.v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, DV, a.hkv, a.T, 64, BN,
                    CU_TENSOR_MAP_SWIZZLE_128B))
@@ -496,7 +505,7 @@ static cudaError_t launch_fwd_impl(const AttnArgs& a, cudaStream_t st) {
   if (e != cudaSuccess) return e;
   const int64_t grid = int64_t(a.num_tiles) * a.hq;
   if (grid == 0) return cudaSuccess;
-  attn_fwd_tc_kernel<DQK, DV><<<unsigned(grid), 192, Cfg::kSmem, st>>>(p);
+  attn_fwd_tc_kernel<DQK, DV><<<unsigned(grid), 224, Cfg::kSmem, st>>>(p);
   return cudaGetLastError();
 }
 
