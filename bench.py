@@ -300,13 +300,18 @@ def ulysses_measure(r: Runner, steps: int = 3, warmup: int = 2) -> dict:
 def linear_measure(dev, steps: int = 5, warmup: int = 3) -> dict:
     """Decayed linear attention with AllGather CP (cp_lin_attn_fwd) on a
     long-sequence configuration: S = 64K tokens, 16 heads of 128, C = 8
-    contiguous pieces, bf16, decays alpha = exp(g) in (0.39, 0.95).  The
-    kernels run FP32 FMAs on the CUDA cores: the roofline is the FP32 FMA
-    peak of the unit counts (152 SMs x 128 lanes x 2 FLOP) at the maximum SM
-    clock."""
+    contiguous pieces, bf16, decays alpha = exp(g) in (0.39, 0.95).  Its three
+    passes run on the tensor cores (block states, output) and as a plain scan
+    (the decayed prefix over the gathered states); what bounds them is HBM,
+    so the roofline counts the bytes the method moves: the state pass reads
+    k and v and writes one D x D state per (block, head); the prefix reads the
+    states and writes the initial states; the output pass reads q, k, v and
+    the initial states and writes o.  Tensor FLOPs of the chunked form are
+    reported beside it."""
     import context_long_sequence_zigzag_gb300 as cpa
 
-    T, H, D, C, B = 65536, 16, 128, 8, 64
+    T, H, D, C = 65536, 16, 128, 8
+    BLOCK, CHUNK = 512, 128  # tokens per parallel block, tokens per chunk
     gen = torch.Generator(device=dev).manual_seed(7)
     q = (torch.randn(T, H, D, device=dev, generator=gen) * 0.5).to(torch.bfloat16)
     k = (torch.randn(T, H, D, device=dev, generator=gen) * 0.5).to(torch.bfloat16)
@@ -325,18 +330,20 @@ def linear_measure(dev, steps: int = 5, warmup: int = 3) -> dict:
             times.append((a, b))
     torch.cuda.synchronize()
     ms = statistics.mean(a.elapsed_time(b) for a, b in times)
-    # chunked form per token and head: local state 2*D*D, intra-chunk scores
-    # and their product with V (B/2 visible keys on average) 2*(B/2)*D each,
-    # initial-state term 2*D*D, state update 2*D*D
-    flops = float(T) * H * (6 * D * D + B * 2 * D)
-    tf = flops / (ms * 1e-3) / 1e12
-    peak = 152 * 128 * 2 * 2.07e9 / 1e12
+    nblocks = C * -(-(T // C) // BLOCK)
+    state_bytes = nblocks * H * D * D * 4
+    nbytes = T * H * D * 2 * (2 + 3 + 1) + 4 * state_bytes
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    peaks, _ = load_peaks()
+    peak_gbs = float(peaks.get("hbm_gbs", FALLBACK["hbm_gbs"]))
+    # per 128-token chunk and head: Q K^T, A' V, Q H and the state update in
+    # the output pass, the state update again in the state pass (2*C*D*D each)
+    flops = float(T // CHUNK) * H * 5 * 2 * CHUNK * D * D
     return {"config": {"total_tokens": T, "heads": H, "head_dim": D, "cp_size": C, "layout": "contiguous",
                        "dtype": "bf16"},
-            "ms": round(ms, 3), "tflops": round(tf, 2),
-            "roofline": {"bound": "alu", "achieved": round(tf, 2), "peak": round(peak, 1), "unit": "TFLOP/s",
-                         "frac": round(tf / peak, 4),
-                         "peak_kind": "FP32 FMA, 152 SMs x 128 lanes x 2 FLOP x 2.07 GHz (unit counts)"}}
+            "ms": round(ms, 3), "tensor_tflops": round(flops / (ms * 1e-3) / 1e12, 2),
+            "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": round(peak_gbs, 1), "unit": "GB/s",
+                         "frac": round(gbs / peak_gbs, 4), "traffic": None, "algorithmic_bytes": nbytes}}
 
 
 def e2e_measure(r: Runner, steps: int, warmup: int):

@@ -31,6 +31,7 @@ SOURCES = [
     "attn_fwd_sm103.cu",
     "attn_bwd_sm103.cu",
     "linear_attn.cu",
+    "linear_attn_tc.cu",
 ]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",

@@ -967,7 +967,8 @@ cp_status_t cp_lin_attn_fwd(const cp_desc_t* d, const void* q, const void* k, co
           cudaSuccess)
     return CP_ERR_CUDA;
   return launch_lin_attn(reinterpret_cast<const LinBlock*>(base + L.blocks), int32_t(B.blocks.size()),
-                         reinterpret_cast<const int32_t*>(base + L.seq_begin), m.S, d->hq, d->d_qk, d->d_v, d->scale,
+                         reinterpret_cast<const int32_t*>(base + L.seq_begin), m.S, d->hq, d->total_tokens, d->d_qk,
+                         d->d_v, d->scale,
                          d->dtype, q, k, v, g, reinterpret_cast<float*>(base + L.states),
                          reinterpret_cast<float*>(base + L.init), o, cs) == cudaSuccess
              ? CP_OK

@@ -98,9 +98,18 @@ struct LinBlock {
   int32_t len;   // tokens
 };
 size_t lin_output_smem(int32_t Dk, int32_t Dv);
+// T = rows of q, k, v, o ([T, H, D] token-major)
 cudaError_t launch_lin_attn(const LinBlock* blocks, int32_t nblocks, const int32_t* seq_begin, int32_t S, int32_t H,
-                            int32_t Dk, int32_t Dv, float scale, int32_t dtype, const void* q, const void* k,
-                            const void* v, const float* g, float* states, float* init, void* o, cudaStream_t st);
+                            int64_t T, int32_t Dk, int32_t Dv, float scale, int32_t dtype, const void* q,
+                            const void* k, const void* v, const float* g, float* states, float* init, void* o,
+                            cudaStream_t st);
+// tensor-core block-state and block-output passes (bf16, 128-wide heads)
+bool lin_tc_supported(int32_t dtype, int32_t Dk, int32_t Dv);
+cudaError_t launch_lin_state_tc(const LinBlock* blocks, int32_t nblocks, int32_t H, int64_t T, const void* k,
+                                const void* v, const float* g, float* states, cudaStream_t st);
+cudaError_t launch_lin_output_tc(const LinBlock* blocks, int32_t nblocks, int32_t H, int64_t T, float scale,
+                                 const void* q, const void* k, const void* v, const float* g, const float* init,
+                                 void* o, cudaStream_t st);
 
 // Ulysses re-layout: perm[s] = global row of sharded row s (T entries, device).
 cudaError_t launch_ulysses_a2a(const int32_t* perm, int64_t T, int32_t C, int64_t chunk_bytes, const void* in,

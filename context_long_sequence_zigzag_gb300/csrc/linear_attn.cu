@@ -19,8 +19,9 @@
 //   lin_output_kernel — per (block, head): chunked decayed attention of the
 //                        block started from init_b, i.e. the local output plus
 //                        the page's correction, in one pass.
-// FP32 CUDA-core arithmetic, register-tiled (head dims multiples of 8, up to
-// 128); bf16 or fp32 tensors.
+// Here: FP32 CUDA-core arithmetic, register-tiled (head dims multiples of 8,
+// up to 128), bf16 or fp32 tensors.  bf16 with 128-wide heads takes the
+// tensor-core state and output passes of linear_attn_tc.cu instead.
 #include <cuda_bf16.h>
 
 #include "internal.h"
@@ -104,22 +105,27 @@ __global__ void __launch_bounds__(kLinThreads) lin_state_kernel(const LinBlock* 
       for (int j = 0; j < 8; ++j) out[(ty * 8 + i) * Dv + tx * 8 + j] = acc[i][j];
 }
 
-// per (sequence, head): blocks of sequence s in order are [seq_begin[s], seq_begin[s+1])
-__global__ void __launch_bounds__(kLinThreads) lin_prefix_kernel(const LinBlock* __restrict__ blocks,
-                                                                  const int32_t* __restrict__ seq_begin, int32_t H,
-                                                                  int32_t DD, const float* __restrict__ g,
-                                                                  const float* __restrict__ states,
-                                                                  float* __restrict__ init) {
-  const int s = blockIdx.x / H, h = blockIdx.x - (blockIdx.x / H) * H;
+// One thread per (sequence, head, state element): blocks of sequence s in
+// order are [seq_begin[s], seq_begin[s+1]); the scan over them is serial per
+// element, the elements are spread over the whole grid.
+constexpr int kPrefixThreads = 256;
+__global__ void __launch_bounds__(kPrefixThreads) lin_prefix_kernel(const LinBlock* __restrict__ blocks,
+                                                                     const int32_t* __restrict__ seq_begin, int32_t H,
+                                                                     int32_t DD, const float* __restrict__ g,
+                                                                     const float* __restrict__ states,
+                                                                     float* __restrict__ init) {
+  const int per_sh = (DD + kPrefixThreads - 1) / kPrefixThreads;  // CTAs per (sequence, head)
+  const int sh = blockIdx.x / per_sh;
+  const int e = (blockIdx.x - sh * per_sh) * kPrefixThreads + threadIdx.x;
+  if (e >= DD) return;
+  const int s = sh / H, h = sh - (sh / H) * H;
   const float gh = g[h];
   const int b0 = seq_begin[s], b1 = seq_begin[s + 1];
-  for (int e = threadIdx.x; e < DD; e += blockDim.x) {
-    float cur = 0.f;
-    for (int b = b0; b < b1; ++b) {
-      const int64_t idx = (int64_t(b) * H + h) * DD + e;
-      init[idx] = cur;
-      cur = __expf(gh * float(blocks[b].len)) * cur + states[idx];
-    }
+  float cur = 0.f;
+  for (int b = b0; b < b1; ++b) {
+    const int64_t idx = (int64_t(b) * H + h) * DD + e;
+    init[idx] = cur;
+    cur = __expf(gh * float(blocks[b].len)) * cur + __ldcs(states + idx);
   }
 }
 
@@ -250,11 +256,21 @@ size_t lin_output_smem(int32_t Dk, int32_t Dv) {
 }
 
 cudaError_t launch_lin_attn(const LinBlock* blocks, int32_t nblocks, const int32_t* seq_begin, int32_t S, int32_t H,
-                            int32_t Dk, int32_t Dv, float scale, int32_t dtype, const void* q, const void* k,
-                            const void* v, const float* g, float* states, float* init, void* o, cudaStream_t st) {
+                            int64_t T, int32_t Dk, int32_t Dv, float scale, int32_t dtype, const void* q,
+                            const void* k, const void* v, const float* g, float* states, float* init, void* o,
+                            cudaStream_t st) {
   if (Dk > 128 || Dv > 128 || Dk % 8 || Dv % 8) return cudaErrorInvalidValue;
   const unsigned grid = unsigned(int64_t(nblocks) * H);
   if (grid == 0) return cudaSuccess;
+  const int per_sh = (Dk * Dv + kPrefixThreads - 1) / kPrefixThreads;
+  if (lin_tc_supported(dtype, Dk, Dv)) {
+    cudaError_t e = launch_lin_state_tc(blocks, nblocks, H, T, k, v, g, states, st);
+    if (e != cudaSuccess) return e;
+    lin_prefix_kernel<<<unsigned(int64_t(S) * H * per_sh), kPrefixThreads, 0, st>>>(blocks, seq_begin, H, Dk * Dv, g,
+                                                                                   states, init);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    return launch_lin_output_tc(blocks, nblocks, H, T, scale, q, k, v, g, init, o, st);
+  }
   const size_t sm_state = state_smem(Dk, Dv), sm_out = lin_output_smem(Dk, Dv);
   auto run = [&](auto ks, auto ko, auto tag) -> cudaError_t {
     using E = decltype(tag);
@@ -264,7 +280,8 @@ cudaError_t launch_lin_attn(const LinBlock* blocks, int32_t nblocks, const int32
       return e;
     ks<<<grid, kLinThreads, sm_state, st>>>(blocks, H, Dk, Dv, static_cast<const E*>(k), static_cast<const E*>(v), g,
                                             states);
-    lin_prefix_kernel<<<unsigned(S * H), kLinThreads, 0, st>>>(blocks, seq_begin, H, Dk * Dv, g, states, init);
+    lin_prefix_kernel<<<unsigned(int64_t(S) * H * per_sh), kPrefixThreads, 0, st>>>(blocks, seq_begin, H, Dk * Dv, g,
+                                                                                   states, init);
     ko<<<grid, kLinThreads, sm_out, st>>>(blocks, H, Dk, Dv, scale, static_cast<const E*>(q),
                                           static_cast<const E*>(k), static_cast<const E*>(v), g, init,
                                           static_cast<E*>(o));

@@ -77,3 +77,24 @@ def test_cp_size_does_not_change_the_result():
     a, _, _ = _case([1000, 24], H=2, Dk=64, Dv=64, C=1, dtype=torch.float32, seed=44)
     b, _, _ = _case([1000, 24], H=2, Dk=64, Dv=64, C=8, dtype=torch.float32, seed=44)
     assert _rel(b, a) < 1e-5
+
+
+def test_bf16_full_size_sampled_heads():
+    """The configuration the benchmark times: one 64K-token sequence, 16 heads
+    of 128, C = 8 contiguous pieces, bf16.  The float64 recurrence runs over
+    the whole sequence for two sampled heads (the first and the last)."""
+    T, H, D, C = 65536, 16, 128, 8
+    cu = [0, T]
+    gen = torch.Generator().manual_seed(45)
+    q = (torch.randn(T, H, D, generator=gen) * 0.5).to(torch.bfloat16)
+    k = (torch.randn(T, H, D, generator=gen) * 0.5).to(torch.bfloat16)
+    v = torch.randn(T, H, D, generator=gen).to(torch.bfloat16)
+    g = -torch.rand(H, generator=gen) * 0.9 - 0.05
+    scale = D ** -0.5
+    prob = cpa.Problem(T, H, H, D, D, C, "contiguous", cu, True, scale, "blocked", torch.bfloat16)
+    # contiguous pieces of one sequence: sharded order is global order
+    o = cpa.cp_lin_attn_fwd(prob, q.cuda(), k.cuda(), v.cuda(), g.cuda()).cpu()
+    heads = [0, H - 1]
+    sel = lambda t: t[:, heads].double().numpy()
+    ref = oracle.linear_attn_recurrent(sel(q), sel(k), sel(v), cu, g[heads].double().numpy(), scale)
+    assert _rel(sel(o), ref) < 2e-2
