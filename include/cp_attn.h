@@ -263,8 +263,12 @@ cp_status_t cp_ulysses_attn_bwd(const cp_desc_t* desc, const void* q, const void
  *               at most 512 tokens, the unit of parallel work, and the prefix
  *               runs over the blocks of a sequence in order — ranks in order,
  *               blocks in order inside a rank)
- * Arithmetic is FP32 on the CUDA cores.  CP_ERR_UNSUPPORTED for another
- * layout, non-causal, or head dims above 128 or not multiples of 8. */
+ * bf16 with d_qk == d_v == 128 runs the block states and block outputs as
+ * tcgen05 MMAs in chunks of 128 tokens, with fp32 accumulation and the
+ * carried state in fp32.  The decayed score matrix, the decay-weighted keys
+ * and the state are rounded to bf16 as MMA operands.  Every other shape runs
+ * FP32 arithmetic on the CUDA cores.  CP_ERR_UNSUPPORTED for another layout,
+ * non-causal, or head dims above 128 or not multiples of 8. */
 cp_status_t cp_lin_attn_fwd(const cp_desc_t* desc, const void* q, const void* k, const void* v,
                             const float* g, void* o,
                             void* workspace, size_t workspace_bytes, cp_stream_t stream);
