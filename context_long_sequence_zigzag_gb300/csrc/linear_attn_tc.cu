@@ -56,13 +56,16 @@ struct LinTcParams {
 
 // Scales the 128 bf16 of row r of a [128 x 128] 128B-swizzled tile by w in
 // place.  The swizzle only permutes 16-byte chunks inside a row, so the row
-// is the same 2 x 128 bytes whatever the permutation.
+// is the same 2 x 128 bytes whatever the permutation.  Thread r starts at
+// chunk r % 8: the rows of a warp are 128 bytes apart, so visiting the same
+// chunk index in every row would put all 32 lanes on the same four banks.
 __device__ __forceinline__ void scale_row_bf16(uint8_t* tile, int r, float w) {
 #pragma unroll
   for (int p = 0; p < 2; ++p) {
     uint4* row = reinterpret_cast<uint4*>(tile + p * kPanel + r * 128);
 #pragma unroll
-    for (int q = 0; q < 8; ++q) {
+    for (int qq = 0; qq < 8; ++qq) {
+      const int q = (qq + r) & 7;
       uint4 u = row[q];
       uint32_t* w32 = reinterpret_cast<uint32_t*>(&u);
 #pragma unroll
@@ -327,18 +330,32 @@ __global__ void __launch_bounds__(kOutThreads, 1) lin_output_tc_kernel(const __g
     constexpr uint32_t idQH = ptx::idesc_bf16_f32(kC, kD, false, true);    // K-major x MN-major
     constexpr uint32_t idAV = ptx::idesc_bf16_f32(kC, kD, false, true);    // TMEM x MN-major
     constexpr uint32_t idKV = ptx::idesc_bf16_f32(kD, kD, true, true);     // MN-major x MN-major
+    // Q K^T of chunk c+1 needs only that chunk's loads: it is issued right
+    // after chunk c's A' V (which it overwrites in TMEM after, in pipe
+    // order), so it runs while the threads write chunk c's output.  Q H has
+    // to wait for the restaged state.
+    auto issue_qk = [&](int c) {
+      const uint32_t sQ = sbase + (c & 1) * kStage;
+      const uint64_t qd = ptx::sdesc_sw128(sQ, 16, 1024), kdk = ptx::sdesc_sw128(sQ + kTile, 16, 1024);
+#pragma unroll
+      for (int kk = 0; kk < kD / 16; ++kk) ptx::mma_ss_w(tA, qd + kmajor_adv(kk), kdk + kmajor_adv(kk), idQK, kk > 0);
+    };
     bool ok = true;
+    if (nch > 0) {
+      ok = ptx::mbar_wait_w(bar_full(0), 0, kLinSiteFull, wctx);
+      if (ok) {
+        ptx::tc_fence_after();
+        issue_qk(0);
+      }
+    }
     for (int c = 0; ok && c < nch; ++c) {
       const int st = c & 1;
       const uint32_t sQ = sbase + st * kStage, sK = sQ + kTile, sV = sQ + 2 * kTile;
-      ok = ptx::mbar_wait_w(bar_full(st), (c >> 1) & 1, kLinSiteFull, wctx) &&
-           ptx::mbar_wait_w(bar_hb, c & 1, kLinSiteHb, wctx);
+      ok = ptx::mbar_wait_w(bar_hb, c & 1, kLinSiteHb, wctx);
       if (!ok) break;
       ptx::tc_fence_after();
-      const uint64_t qd = ptx::sdesc_sw128(sQ, 16, 1024), kdk = ptx::sdesc_sw128(sK, 16, 1024);
+      const uint64_t qd = ptx::sdesc_sw128(sQ, 16, 1024);
       const uint64_t hd = ptx::sdesc_sw128(sbase + offHb, kPanel, 1024);
-#pragma unroll
-      for (int kk = 0; kk < kD / 16; ++kk) ptx::mma_ss_w(tA, qd + kmajor_adv(kk), kdk + kmajor_adv(kk), idQK, kk > 0);
 #pragma unroll
       for (int kk = 0; kk < kD / 16; ++kk) ptx::mma_ss_w(tY, qd + kmajor_adv(kk), hd + mnmajor_adv(kk), idQH, kk > 0);
       ptx::mma_commit_w(bar_qk);
@@ -352,6 +369,12 @@ __global__ void __launch_bounds__(kOutThreads, 1) lin_output_tc_kernel(const __g
       for (int kk = 0; kk < kC / 16; ++kk) ptx::mma_ss_w(tH, kdm + mnmajor_adv(kk), vd + mnmajor_adv(kk), idKV, 1);
       ptx::mma_commit_w(bar_xh);
       ptx::mma_commit_w(bar_empty(st));
+      if (c + 1 < nch) {
+        ok = ptx::mbar_wait_w(bar_full((c + 1) & 1), ((c + 1) >> 1) & 1, kLinSiteFull, wctx);
+        if (!ok) break;
+        ptx::tc_fence_after();
+        issue_qk(c + 1);
+      }
     }
     if (!ok) {
       volatile int no_abort = 0;
@@ -365,16 +388,19 @@ __global__ void __launch_bounds__(kOutThreads, 1) lin_output_tc_kernel(const __g
     const uint32_t lane_base = uint32_t(warp * 32) << 16;
     uint8_t* Hb = smem + offHb;
     bool ok = true;
-    // carried-in state -> TMEM (fp32) and the bf16 copy for the first Q H
+    // carried-in state -> TMEM (fp32) and the bf16 copy for the first Q H;
+    // all 32 loads of the row are issued before any is used
     {
-      const float* src = p.init + ((int64_t(b) * p.H + h) * kD + r) * kD;
-#pragma unroll 1
+      const float4* src = reinterpret_cast<const float4*>(p.init + ((int64_t(b) * p.H + h) * kD + r) * kD);
+      float4 v4[32];
+#pragma unroll
+      for (int i = 0; i < 32; ++i) v4[i] = __ldcs(src + i);
+#pragma unroll
       for (int c = 0; c < 4; ++c) {
         uint32_t x[32];
-        const float4* s4 = reinterpret_cast<const float4*>(src + c * 32);
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-          const float4 v = __ldg(s4 + i);
+          const float4 v = v4[c * 8 + i];
           x[4 * i] = __float_as_uint(v.x);
           x[4 * i + 1] = __float_as_uint(v.y);
           x[4 * i + 2] = __float_as_uint(v.z);
