@@ -346,6 +346,46 @@ def linear_measure(dev, steps: int = 5, warmup: int = 3) -> dict:
                          "frac": round(gbs / peak_gbs, 4), "traffic": None, "algorithmic_bytes": nbytes}}
 
 
+def other_configs_measure(dev, main_name: str, steps: int = 2, warmup: int = 1) -> dict:
+    """Device throughput of the other standard bf16 problems (S = 16K GQA, the
+    128K-token varlen pack, the S = 256K MLA shape): the same step as the
+    headline (permutes, forward, D pre-pass, dK/dV, dQ, permutes back), the
+    same FLOP rule, and the forward / backward fractions of the bf16 peak.
+    The fp32 S = 256 problem is a correctness case of the CUDA-core path
+    and gets no throughput line."""
+    peaks, _ = load_peaks()
+    burst = float(peaks.get("bf16_tflops", FALLBACK["bf16_tflops"]))
+    out = {}
+    for name in workloads.ORDER:
+        w = workloads.get(name)
+        if name == main_name or w.dtype != "bf16":
+            continue
+        r = Runner(w, dev)
+        for _ in range(warmup):
+            r.step()
+        torch.cuda.synchronize()
+        r.ev.clear()
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0.record()
+        for _ in range(steps):
+            r.step(record=True)
+        t1.record()
+        torch.cuda.synchronize()
+        ms = t0.elapsed_time(t1) / steps
+        fwd_ms, bwd_ms, _, _ = r.kernel_times_ms()
+        f_fwd, f_bwd = w.flops_fwd(), w.flops_bwd()
+        fwd_tf, bwd_tf = f_fwd / (fwd_ms * 1e-3) / 1e12, f_bwd / (bwd_ms * 1e-3) / 1e12
+        out[name] = {"ms_per_step": round(ms, 3), "tflops": round((f_fwd + f_bwd) / (ms * 1e-3) / 1e12, 2),
+                     "fwd_tflops": round(fwd_tf, 2), "bwd_tflops": round(bwd_tf, 2),
+                     "fwd_frac_of_burst": round(fwd_tf / burst, 4), "bwd_frac_of_burst": round(bwd_tf / burst, 4)}
+        status = r.cpa.cp_device_status()
+        if status != 0:
+            raise RuntimeError(f"device wait timeout code {status:#x} ({name})")
+        del r
+        torch.cuda.empty_cache()
+    return out
+
+
 def e2e_measure(r: Runner, steps: int, warmup: int):
     """Same metric through the ABI with host buffers: every step copies its
     inputs (q, k, v, dout) in from pinned host memory and its results (o,
@@ -499,6 +539,8 @@ def run_gpu(args):
     aux = aux_bandwidth(r)
     uly = ulysses_measure(r) if not args.no_ulysses else {"skipped": "--no-ulysses"}
     lin = linear_measure(dev) if not args.no_linear else {"skipped": "--no-linear"}
+    others = (other_configs_measure(dev, w.name) if world == 1 and not args.no_other_configs
+              else {"skipped": "--no-other-configs" if args.no_other_configs else "N > 1"})
 
     peaks, peak_kind = load_peaks()
     peak_sus = float(peaks.get("bf16_tflops_sustained", FALLBACK["bf16_tflops_sustained"]))
@@ -563,6 +605,7 @@ def run_gpu(args):
             "rank_block_counts": cpa.cp_rank_block_counts(r.prob),
             "rank_balance": balance_report(cpa, w),
             "ulysses": uly,
+            "other_configs": others,
             "linear_attention_cp": lin,
         }
         if "ms_per_step" in uly:
@@ -632,6 +675,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-ulysses", action="store_true", help="skip the Ulysses comparison")
     ap.add_argument("--no-linear", action="store_true", help="skip the linear-attention CP measurement")
+    ap.add_argument("--no-other-configs", action="store_true",
+                    help="skip the throughput lines of the other standard problems")
     ap.add_argument("--layout", default=None, choices=["contiguous", "zigzag", "striped"],
                     help="shard layout instead of the workload's own (zigzag for the standard ones)")
     args = ap.parse_args()
