@@ -535,7 +535,9 @@ def run_gpu(args):
         raise RuntimeError(f"device wait timeout code {status:#x}")
     fwd_ms, bwd_ms, dkdv_ms, dq_ms = r.kernel_times_ms()
 
-    e2e_ms, h2d, d2h = e2e_measure(r, max(3, min(args.steps, 10)), 1)
+    # at least 8 steps: one step's H2D before the first and one D2H after the last are
+    # not overlapped, and the per-step number should be the steady state
+    e2e_ms, h2d, d2h = e2e_measure(r, min(max(args.steps, 8), 16), 1)
     aux = aux_bandwidth(r)
     uly = ulysses_measure(r) if not args.no_ulysses else {"skipped": "--no-ulysses"}
     lin = linear_measure(dev) if not args.no_linear else {"skipped": "--no-linear"}
