@@ -486,6 +486,17 @@ def aux_bandwidth(r: "Runner", reps: int = 5) -> dict:
     return out
 
 
+def slowest_rank_ms(ms: float, device) -> float:
+    """The timed region of a multi-rank run lasts as long as its slowest
+    rank: the maximum of every rank's time (any backend; on one rank, ms)."""
+    dist = torch.distributed
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return ms
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def run_gpu(args):
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -525,11 +536,7 @@ def run_gpu(args):
     if world > 1:
         torch.distributed.barrier()
     clk = clocks.stop()
-    ms = t0.elapsed_time(t1) / args.steps
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = slowest_rank_ms(t0.elapsed_time(t1) / args.steps, dev)
     status = cpa.cp_device_status()
     if status != 0:
         raise RuntimeError(f"device wait timeout code {status:#x}")
