@@ -23,7 +23,9 @@
 //     next DQK       dK += dS^T Q (TS)
 //   MMA order S(i), dK(i-1), dP(i), dV(i): the tensor pipe computes dK of
 //   the previous step and dP while the softmax warps turn S into P, and S of
-//   the next step while they turn dP into dS.
+//   the next step while they turn dP into dS.  Q and dO stream through
+//   separate TMA rings (3 and 2 stages for 128-wide heads): a Q stage is
+//   released by dK, a dO stage by dV.
 //
 // attn_bwd_dq_kernel — query-tile-major.  One CTA owns a 128-row query tile
 //   of one head and visits the key tiles of the forward plan; dQ accumulates
@@ -42,7 +44,9 @@
 // TMEM allocator + MMA issuer; the dQ
 // kernel adds warp 10, which issues the dQ MMAs so that waiting for dS never
 // delays S and dP of the next key tile.  MMA-issuing warps run converged and
-// elect one lane per instruction.
+// elect one lane per instruction.  The P and dS loops use packed f32x2
+// arithmetic; dK/dV stages its per-column statistics negated so that a float4
+// of them is two packed addends.
 #include <cuda.h>
 #include <cuda_bf16.h>
 
