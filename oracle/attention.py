@@ -162,42 +162,122 @@ def _rows_by_seq(cu: list, rows: np.ndarray):
         yield cu[s], cu[s + 1], np.nonzero(seq == s)[0]
 
 
+# ---------------------------------------------------------------------------
+# Samplers for long sequences.  They compute the same definitions as
+# attn_forward / attn_backward for selected rows only, in plain PyTorch
+# float64 CPU ops (matrix products and elementwise exp/max/sum spread over the
+# host cores), so that problems of 64K-256K tokens stay within seconds to a
+# minute.  Every selected row still gets its full-row softmax over all of its
+# visible keys in one piece.
+
+def _t64(x):
+    """Exact float64 CPU torch copy of a numpy array or a torch tensor."""
+    import torch
+
+    if isinstance(x, torch.Tensor):
+        return x.detach().to("cpu", torch.float64)
+    return torch.from_numpy(np.ascontiguousarray(x, dtype=np.float64))
+
+
+def _gather_rows(x, idx, h):
+    """x[idx, h] (global rows idx of head h) as float64 torch."""
+    import torch
+
+    if isinstance(x, torch.Tensor):
+        return _t64(x[torch.as_tensor(np.asarray(idx, dtype=np.int64)), h])
+    return _t64(np.asarray(x)[np.asarray(idx, dtype=np.int64), h])
+
+
+class _Scores:
+    """scale * Q K^T into one reused float64 buffer (allocating a fresh
+    multi-hundred-MB matrix per block costs more than the product itself)."""
+
+    def __init__(self):
+        self.buf = None
+
+    def __call__(self, Qs, K, scale: float):
+        import torch
+
+        n, m = Qs.shape[0], K.shape[0]
+        if self.buf is None or self.buf.numel() < n * m:
+            self.buf = torch.empty(max(n * m, 1), dtype=torch.float64)
+        S = self.buf[:n * m].view(n, m)
+        torch.mm(Qs, K.T, out=S)
+        return S.mul_(scale)
+
+
+def _softmax_rows_t(S, qpos, causal: bool):
+    """Row softmax of the scaled scores S [n, m] of queries at sequence
+    positions qpos [n] against the keys at positions 0..m-1 (key j is masked
+    for query i when causal and j > pos(i)).  S is overwritten.  Returns
+    (P, lse); rows that see no key give P = 0 and lse = -inf."""
+    import torch
+
+    n, m = S.shape
+    if m == 0:
+        return S, torch.full((n,), float("-inf"), dtype=torch.float64)
+    if causal:
+        c0 = int(qpos.min())  # keys before the earliest query are visible to every row
+        if c0 < m:
+            j = torch.arange(c0, m)
+            S[:, c0:].masked_fill_(j[None, :] > qpos[:, None], float("-inf"))
+    mx = S.amax(dim=1)
+    empty = torch.isneginf(mx)
+    mx = torch.where(empty, torch.zeros_like(mx), mx)
+    S.sub_(mx[:, None]).exp_()  # masked entries: exp(-inf) = 0
+    l = S.sum(dim=1)
+    lse = torch.where(empty, torch.full_like(mx, float("-inf")), mx + torch.log(l))
+    P = S.div_(torch.where(empty, torch.ones_like(l), l)[:, None])
+    return P, lse
+
+
+def _sampled_rows_forward(q, k, v, cu, scale, rows, h, kvh, causal, chunk, dout=None):
+    """Yields (positions in rows, P, O, Q, K, V, dO) per chunk of the selected
+    rows of one sequence at a time, for query head h / kv head kvh."""
+    import torch
+
+    scores = _Scores()
+    for a, b, idx in _rows_by_seq(cu, rows):
+        pos_all = rows[idx] - a
+        m_seq = int(pos_all.max()) + 1 if causal else b - a
+        K = _t64(k[a:a + m_seq, kvh])
+        V = _t64(v[a:a + m_seq, kvh])
+        for c0 in range(0, len(idx), chunk):
+            sel = idx[c0:c0 + chunk]
+            pos = torch.as_tensor(rows[sel] - a)
+            m = int(pos.max()) + 1 if causal else b - a
+            Qs = _gather_rows(q, rows[sel], h)
+            P, lse = _softmax_rows_t(scores(Qs, K[:m], scale), pos, causal)
+            dOs = _gather_rows(dout, rows[sel], h) if dout is not None else None
+            yield sel, P, lse, Qs, K[:m], V[:m], dOs
+
+
 def attn_forward_rows(q, k, v, cu_seqlens, scale: float, rows: Sequence[int],
                       heads: Iterable[int], causal: bool = True, gqa: str = "blocked",
-                      chunk: int = 64):
+                      chunk: int = 128):
     """Forward for selected global query rows and query heads only.
 
     Every selected row gets the full-row softmax over its visible keys; rows
-    of one sequence are handled together as a small matrix product.
-    Returns o [n_rows, n_heads, dv] and lse [n_heads, n_rows].
+    of one sequence are handled together as a matrix product.
+    Returns o [n_rows, n_heads, dv] and lse [n_heads, n_rows] (numpy float64).
     """
     rows = np.asarray(rows, dtype=np.int64)
     heads = list(heads)
     hq, hkv = q.shape[1], k.shape[1]
     cu = _cu(cu_seqlens)
-    dv = v.shape[2]
-    o = np.zeros((len(rows), len(heads), dv))
+    o = np.zeros((len(rows), len(heads), v.shape[2]))
     lse = np.full((len(heads), len(rows)), -np.inf)
     for hi, h in enumerate(heads):
         kvh = kv_head(h, hq, hkv, gqa)
-        for a, b, idx in _rows_by_seq(cu, rows):
-            K = _f64(k[a:b, kvh])
-            V = _f64(v[a:b, kvh])
-            for c0 in range(0, len(idx), chunk):
-                sel = idx[c0:c0 + chunk]
-                pos = rows[sel] - a
-                Qs = _f64(q[rows[sel], h])
-                S = scale * (Qs @ K.T)
-                vis = (np.arange(b - a)[None, :] <= pos[:, None]) if causal else np.ones_like(S, dtype=bool)
-                P, l = _softmax_rows(S, vis)
-                o[sel, hi] = P @ V
-                lse[hi, sel] = l
+        for sel, P, l, _, _, V, _ in _sampled_rows_forward(q, k, v, cu, scale, rows, h, kvh, causal, chunk):
+            o[sel, hi] = (P @ V).numpy()
+            lse[hi, sel] = l.numpy()
     return o, lse
 
 
 def attn_backward_dq_rows(q, k, v, dout, cu_seqlens, scale: float, rows: Sequence[int],
                           heads: Iterable[int], causal: bool = True, gqa: str = "blocked",
-                          chunk: int = 64):
+                          chunk: int = 128):
     """dq for selected global query rows / query heads: [n_rows, n_heads, dk]."""
     rows = np.asarray(rows, dtype=np.int64)
     heads = list(heads)
@@ -206,63 +286,68 @@ def attn_backward_dq_rows(q, k, v, dout, cu_seqlens, scale: float, rows: Sequenc
     out = np.zeros((len(rows), len(heads), q.shape[2]))
     for hi, h in enumerate(heads):
         kvh = kv_head(h, hq, hkv, gqa)
-        for a, b, idx in _rows_by_seq(cu, rows):
-            K = _f64(k[a:b, kvh])
-            V = _f64(v[a:b, kvh])
-            for c0 in range(0, len(idx), chunk):
-                sel = idx[c0:c0 + chunk]
-                pos = rows[sel] - a
-                Qs, dOs = _f64(q[rows[sel], h]), _f64(dout[rows[sel], h])
-                S = scale * (Qs @ K.T)
-                vis = (np.arange(b - a)[None, :] <= pos[:, None]) if causal else np.ones_like(S, dtype=bool)
-                P, _ = _softmax_rows(S, vis)
-                O = P @ V
-                Di = (dOs * O).sum(axis=1)
-                dP = dOs @ V.T
-                dS = P * (dP - Di[:, None])
-                out[sel, hi] = scale * (dS @ K)
+        for sel, P, _, _, K, V, dOs in _sampled_rows_forward(q, k, v, cu, scale, rows, h, kvh, causal, chunk,
+                                                               dout=dout):
+            O = P @ V
+            Di = (dOs * O).sum(dim=1)
+            dS = P * (dOs @ V.T - Di[:, None])
+            out[sel, hi] = (scale * (dS @ K)).numpy()
     return out
 
 
 def attn_backward_dkdv_rows(q, k, v, dout, cu_seqlens, scale: float, keys: Sequence[int],
-                            kv_heads: Iterable[int], causal: bool = True, gqa: str = "blocked"):
+                            kv_heads: Iterable[int], causal: bool = True, gqa: str = "blocked",
+                            row_block: int = 1024):
     """dk, dv for selected global key rows and key/value heads.
 
-    Needs every query row that sees a selected key (its lse and D), so the
-    cost grows with the distance of the key from the end of its sequence.
-    Returns dk [n_keys, n_kv, dk], dv [n_keys, n_kv, dv].
+    dk_j and dv_j sum over every query row i that sees key j, and each such
+    row needs its own lse_i and D_i = dO_i . o_i, i.e. its whole forward row.
+    The query rows of a sequence, from its earliest selected key on, are
+    therefore visited in blocks of row_block consecutive rows; each block
+    takes its full visible key range (keys past the block's last row are
+    masked for all of it), computes P, o and D, and adds the selected keys'
+    terms.  Memory stays bounded at any sequence length; the cost is that of
+    the forward over those rows.
+    Returns dk [n_keys, n_kv, dk], dv [n_keys, n_kv, dv] (numpy float64).
     """
+    import torch
+
     keys = np.asarray(keys, dtype=np.int64)
     kv_heads = list(kv_heads)
     hq, hkv = q.shape[1], k.shape[1]
     cu = _cu(cu_seqlens)
     seq = _seq_of_rows(cu, keys)
-    dk = np.zeros((len(keys), len(kv_heads), q.shape[2]))
-    dv = np.zeros((len(keys), len(kv_heads), v.shape[2]))
+    dk = torch.zeros(len(keys), len(kv_heads), q.shape[2], dtype=torch.float64)
+    dv = torch.zeros(len(keys), len(kv_heads), v.shape[2], dtype=torch.float64)
+    scores = _Scores()
     for s in np.unique(seq):
         a, b = cu[s], cu[s + 1]
+        L = b - a
         sel = np.nonzero(seq == s)[0]
-        jmin = int(keys[sel].min()) if causal else a
+        kpos = torch.as_tensor(keys[sel] - a)
+        r_start = int(kpos.min()) if causal else 0  # earlier rows see none of the selected keys
         for ki, kvh in enumerate(kv_heads):
-            K = _f64(k[a:b, kvh])
-            V = _f64(v[a:b, kvh])
+            K = _t64(k[a:b, kvh])
+            V = _t64(v[a:b, kvh])
+            Vsel = V[kpos]
             for h in _heads_of(kvh, hq, hkv, gqa):
-                # every query row that can see any selected key of this sequence
-                rlo = jmin - a
-                Qb = _f64(q[a + rlo:b, h])
-                dOb = _f64(dout[a + rlo:b, h])
-                L = b - a
-                S = scale * (Qb @ K.T)
-                P, _ = _softmax_rows(S, _vis_block(rlo, L, L, causal))
-                Ob = P @ V
-                Db = (dOb * Ob).sum(axis=1)
-                for idx in sel:
-                    j = int(keys[idx]) - a
-                    dPj = dOb @ V[j]
-                    dSj = P[:, j] * (dPj - Db)
-                    dk[idx, ki] += scale * (dSj @ Qb)
-                    dv[idx, ki] += P[:, j] @ dOb
-    return dk, dv
+                Q = _t64(q[a + r_start:b, h])
+                dO = _t64(dout[a + r_start:b, h])
+                for r0 in range(r_start, L, row_block):
+                    r1 = min(L, r0 + row_block)
+                    m = r1 if causal else L
+                    Qb, dOb = Q[r0 - r_start:r1 - r_start], dO[r0 - r_start:r1 - r_start]
+                    P, _ = _softmax_rows_t(scores(Qb, K[:m], scale), torch.arange(r0, r1), causal)
+                    Db = (dOb * (P @ V[:m])).sum(dim=1)
+                    seen = kpos < m  # selected keys some row of this block can see
+                    if not bool(seen.any()):
+                        continue
+                    Pj = P[:, kpos[seen]]
+                    dSj = Pj * (dOb @ Vsel[seen].T - Db[:, None])
+                    tgt = torch.as_tensor(sel)[seen]
+                    dk[tgt, ki] += scale * (dSj.T @ Qb)
+                    dv[tgt, ki] += Pj.T @ dOb
+    return dk.numpy(), dv.numpy()
 
 
 def attn_forward_keyset(q, k, v, cu_seqlens, scale: float, key_mask, causal: bool = True,

@@ -5,11 +5,16 @@ pack, the S=256K MLA-shaped problem) runs through the C ABI exactly as the
 benchmark step does: shard permutation, fused forward, D pre-pass, dK/dV and
 dQ kernels, inverse permutation.  The float64 oracle then checks seeded
 samples:
-  * o and lse on sampled query rows for the query heads of the first and
-    last GQA group (max-abs 2e-2 / 1e-3),
-  * dq on the same rows (relative Frobenius 2e-2),
-  * dk, dv on sampled keys near the end of their sequence, where the set of
-    queries that see a key is small enough for the oracle (rel. Frobenius 2e-2),
+  * every head group (the query heads that share one key/value head) gets
+    its own 256 seeded query rows; on them o (max-abs 2e-2 and relative
+    Frobenius 2e-2), lse (max-abs 1e-3) and dq (relative Frobenius 2e-2);
+  * dk, dv (relative Frobenius 2e-2) on 256 seeded keys spread over the whole
+    token stream, for the first and the last key/value head.  Such keys are
+    seen by the queries of every later chunk of their sequence, on every
+    virtual rank, so these sums run over long unmasked runs of many query
+    tiles.  The oracle computes lse and D for every query row that sees them
+    (row blocks, full softmax rows);
+  * on the varlen pack, additionally every key of the shortest sequence;
 and, over every row, the exact identities sum_j dk_j = 0 and
 sum_j dv_j = sum over the group's heads of sum_i dout_i per sequence.
 """
@@ -40,9 +45,24 @@ FULL = [
     "bf16_mla_s256k_h64_dqk192_dv128_c32_zigzag",
 ]
 
+ROWS_PER_GROUP = 256
+KEYS = 256
+
 
 def _f64(t):
     return t.detach().to("cpu", torch.float64).numpy()
+
+
+def _check_keys(name, inp, cu, w, keys, kvs, dk, dv):
+    keys = np.asarray(keys, dtype=np.int64)
+    dk_ref, dv_ref = oracle.attn_backward_dkdv_rows(inp["q"], inp["k"], inp["v"], inp["dout"], cu, w.scale, keys,
+                                                    kvs)
+    keys_t = torch.from_numpy(keys).cuda()
+    for i, kv in enumerate(kvs):
+        e_dk = rel_fro(_f64(dk.index_select(0, keys_t)[:, kv]), dk_ref[:, i])
+        e_dv = rel_fro(_f64(dv.index_select(0, keys_t)[:, kv]), dv_ref[:, i])
+        assert e_dk < BF16_GRAD_RFRO, (name, kv, e_dk)
+        assert e_dv < BF16_GRAD_RFRO, (name, kv, e_dv)
 
 
 @pytest.mark.parametrize("name", FULL)
@@ -65,42 +85,34 @@ def test_full_size_sampled_parity(name):
     assert cpa.cp_device_status() == 0
     del sh, o_s, dq_s, dk_s, dv_s, lse_s, dps
 
-    # query heads of the first and last GQA group, as a sub-problem
     G = w.hq // w.hkv
+    # ---- o, lse, dq: every head group, its own seeded rows
+    for kv in range(w.hkv):
+        heads = [kv * G + g for g in range(G)]
+        rows = workloads.sample_rows(T, ROWS_PER_GROUP, w.seed + 1000 + kv)
+        rows_t = torch.from_numpy(rows).cuda()
+        o_ref, lse_ref = oracle.attn_forward_rows(inp["q"], inp["k"], inp["v"], cu, w.scale, rows, heads)
+        o_gpu = _f64(o.index_select(0, rows_t)[:, heads])
+        lse_gpu = _f64(lse[heads][:, rows_t])
+        assert max_abs(o_gpu, o_ref) < BF16_O_ATOL, (kv, max_abs(o_gpu, o_ref))
+        assert rel_fro(o_gpu, o_ref) < BF16_GRAD_RFRO, (kv, rel_fro(o_gpu, o_ref))
+        assert max_abs(lse_gpu, lse_ref) < BF16_LSE_ATOL, (kv, max_abs(lse_gpu, lse_ref))
+        dq_ref = oracle.attn_backward_dq_rows(inp["q"], inp["k"], inp["v"], inp["dout"], cu, w.scale, rows, heads)
+        e_dq = rel_fro(_f64(dq.index_select(0, rows_t)[:, heads]), dq_ref)
+        assert e_dq < BF16_GRAD_RFRO, (kv, e_dq)
+
+    # ---- dk, dv: keys spread over the whole stream, first and last kv head
     kvs = sorted({0, w.hkv - 1})
-    heads = [kv * G + g for kv in kvs for g in range(G)]
-    qs, dos = _f64(inp["q"][:, heads]), _f64(inp["dout"][:, heads])
-    ks, vs = _f64(inp["k"][:, kvs]), _f64(inp["v"][:, kvs])
-    nh = len(heads)
-
-    # ---- forward and dq on sampled rows
-    n_rows = 256 if T <= 65536 else 96
-    rows = workloads.sample_rows(T, n_rows, w.seed)
-    o_ref, lse_ref = oracle.attn_forward_rows(qs, ks, vs, cu, w.scale, rows, range(nh))
-    rows_t = torch.from_numpy(rows).cuda()
-    o_gpu = _f64(o.index_select(0, rows_t)[:, heads])
-    lse_gpu = _f64(lse[heads][:, rows_t])
-    assert max_abs(o_gpu, o_ref) < BF16_O_ATOL
-    assert max_abs(lse_gpu, lse_ref) < BF16_LSE_ATOL
-    dq_ref = oracle.attn_backward_dq_rows(qs, ks, vs, dos, cu, w.scale, rows, range(nh))
-    assert rel_fro(_f64(dq.index_select(0, rows_t)[:, heads]), dq_ref) < BF16_GRAD_RFRO
-
-    # ---- dk, dv on sampled keys near the end of sampled sequences
-    rng = np.random.RandomState(w.seed + 101)
-    nseq = len(cu) - 1
-    seqs = sorted(rng.choice(nseq, size=min(4, nseq), replace=False).tolist())
-    keys = []
-    for s in seqs:
-        a, b = cu[s], cu[s + 1]
-        lo = max(a, b - 160)
-        keys.extend(sorted(rng.choice(np.arange(lo, b), size=min(6, b - lo), replace=False).tolist()))
-    keys = np.asarray(keys, dtype=np.int64)
-    dk_ref, dv_ref = oracle.attn_backward_dkdv_rows(qs, ks, vs, dos, cu, w.scale, keys, range(len(kvs)))
-    keys_t = torch.from_numpy(keys).cuda()
-    assert rel_fro(_f64(dk.index_select(0, keys_t)[:, kvs]), dk_ref) < BF16_GRAD_RFRO
-    assert rel_fro(_f64(dv.index_select(0, keys_t)[:, kvs]), dv_ref) < BF16_GRAD_RFRO
+    _check_keys(name, inp, cu, w, workloads.sample_rows(T, KEYS, w.seed + 101), kvs, dk, dv)
+    lengths = np.diff(cu)
+    if len(lengths) > 1:
+        # every key of the shortest sequence: each of its 2C zigzag chunks,
+        # on every virtual rank, against every query that sees it
+        s = int(np.argmin(np.where(lengths >= 2 * w.cp_size, lengths, np.iinfo(np.int64).max)))
+        _check_keys(name, inp, cu, w, np.arange(cu[s], cu[s + 1]), kvs, dk, dv)
 
     # ---- identities over every row: sum_j dk_j = 0, sum_j dv_j = sum dout
+    nseq = len(cu) - 1
     for s in range(nseq):
         a, b = cu[s], cu[s + 1]
         if b - a < 2:

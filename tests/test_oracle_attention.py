@@ -235,20 +235,33 @@ def test_backward_identities():
     np.testing.assert_allclose(g["D"], np.einsum("thd,thd->ht", dout, g["o"]), atol=1e-13)
 
 
-def test_sampled_rows_agree_with_full():
+@pytest.mark.parametrize("causal,gqa", [(True, "blocked"), (False, "blocked"), (True, "interleaved")])
+def test_sampled_rows_agree_with_full(causal, gqa):
+    """The long-sequence samplers equal the full functions on the selected
+    rows, with row blocks and chunks small enough that every sequence spans
+    several of them (so the blocking itself is exercised)."""
     cu = [0, 90, 91, 200]
     T = 200
     q, k, v = _rand((T, 4, 8), 35), _rand((T, 2, 8), 36), _rand((T, 2, 6), 37)
     dout = _rand((T, 4, 6), 38)
-    g = oracle.attn_backward(q, k, v, dout, cu, 0.4, row_block=32)
-    rows = [0, 17, 89, 90, 91, 150, 199]
+    g = oracle.attn_backward(q, k, v, dout, cu, 0.4, causal=causal, gqa=gqa, row_block=32)
+    rows = [0, 17, 18, 40, 89, 90, 91, 150, 151, 152, 199]
     heads = [0, 3]
-    o, lse = oracle.attn_forward_rows(q, k, v, cu, 0.4, rows, heads)
-    np.testing.assert_allclose(o, g["o"][rows][:, heads], atol=1e-13)
-    np.testing.assert_allclose(lse, g["lse"][heads][:, rows], atol=1e-13)
-    dq = oracle.attn_backward_dq_rows(q, k, v, dout, cu, 0.4, rows, heads)
-    np.testing.assert_allclose(dq, g["dq"][rows][:, heads], atol=1e-12)
-    keys = [5, 80, 89, 90, 120, 199]
-    dk, dv = oracle.attn_backward_dkdv_rows(q, k, v, dout, cu, 0.4, keys, [0, 1])
-    np.testing.assert_allclose(dk, g["dk"][keys], atol=1e-12)
-    np.testing.assert_allclose(dv, g["dv"][keys], atol=1e-12)
+    for chunk in (128, 3):
+        o, lse = oracle.attn_forward_rows(q, k, v, cu, 0.4, rows, heads, causal=causal, gqa=gqa, chunk=chunk)
+        np.testing.assert_allclose(o, g["o"][rows][:, heads], atol=1e-13)
+        np.testing.assert_allclose(lse, g["lse"][heads][:, rows], atol=1e-13)
+        dq = oracle.attn_backward_dq_rows(q, k, v, dout, cu, 0.4, rows, heads, causal=causal, gqa=gqa, chunk=chunk)
+        np.testing.assert_allclose(dq, g["dq"][rows][:, heads], atol=1e-12)
+    keys = [0, 5, 80, 89, 90, 91, 120, 121, 199]
+    for row_block in (1024, 7):
+        dk, dv = oracle.attn_backward_dkdv_rows(q, k, v, dout, cu, 0.4, keys, [0, 1], causal=causal, gqa=gqa,
+                                                row_block=row_block)
+        np.testing.assert_allclose(dk, g["dk"][keys], atol=1e-12)
+        np.testing.assert_allclose(dv, g["dv"][keys], atol=1e-12)
+    # a torch bf16 input (how the GPU tests pass it) gives the same rows as its float64 copy
+    qt = torch.from_numpy(q).to(torch.bfloat16)
+    q64 = qt.to(torch.float64).numpy()
+    o_t, _ = oracle.attn_forward_rows(qt, k, v, cu, 0.4, rows, heads, causal=causal, gqa=gqa)
+    o_n, _ = oracle.attn_forward_rows(q64, k, v, cu, 0.4, rows, heads, causal=causal, gqa=gqa)
+    np.testing.assert_array_equal(o_t, o_n)
