@@ -13,7 +13,7 @@ Functions carry the C names: ``cp_shard_permute``, ``cp_attn_block_fwd``,
 ``cp_lse_merge``, ``cp_attn_fwd``, ``cp_attn_bwd``, ``cp_workspace_size``,
 ``cp_shard_offsets``, ``cp_rank_block_counts``, ``cp_device_status``,
 ``cp_check_bounded_wait``, ``cp_status_string``, ``cp_validate``, ``cp_ulysses_a2a``,
-``cp_ulysses_attn_fwd``, ``cp_ulysses_attn_bwd``.
+``cp_ulysses_attn_fwd``, ``cp_ulysses_attn_bwd``, ``cp_ring_attn_fwd``, ``cp_lin_attn_fwd``.
 """
 
 from __future__ import annotations
@@ -40,14 +40,15 @@ CP_LAYOUT_CONTIGUOUS, CP_LAYOUT_ZIGZAG, CP_LAYOUT_STRIPED = 0, 1, 2
 CP_DT_F32, CP_DT_BF16 = 0, 1
 CP_GQA_BLOCKED, CP_GQA_INTERLEAVED = 0, 1
 CP_OP_FWD, CP_OP_BWD, CP_OP_BLOCK_FWD, CP_OP_PERMUTE, CP_OP_BWD_DKDV, CP_OP_BWD_DQ = 0, 1, 2, 3, 4, 5
-CP_OP_ULYSSES_A2A, CP_OP_ULYSSES_FWD, CP_OP_ULYSSES_BWD, CP_OP_LIN_FWD = 6, 7, 8, 9
+CP_OP_ULYSSES_A2A, CP_OP_ULYSSES_FWD, CP_OP_ULYSSES_BWD, CP_OP_LIN_FWD, CP_OP_RING_FWD = 6, 7, 8, 9, 10
 
 EXPORTED = [
     "cp_status_string", "cp_validate", "cp_workspace_size", "cp_shard_offsets",
     "cp_rank_block_counts", "cp_shard_permute", "cp_attn_block_fwd", "cp_lse_merge",
     "cp_attn_fwd", "cp_attn_bwd", "cp_device_status", "cp_check_bounded_wait",
     "cp_attn_fwd_noalloc", "cp_attn_bwd_prep", "cp_attn_bwd_dkdv", "cp_attn_bwd_dq",
-    "cp_ulysses_a2a", "cp_ulysses_attn_fwd", "cp_ulysses_attn_bwd", "cp_lin_attn_fwd",
+    "cp_ulysses_a2a", "cp_ulysses_attn_fwd", "cp_ulysses_attn_bwd", "cp_lin_attn_fwd", "cp_ring_attn_fwd",
+    "cp_set_debug_checks",
 ]
 
 
@@ -94,6 +95,8 @@ _sigs = {
     "cp_ulysses_attn_fwd": (ctypes.c_int, [_DP, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
     "cp_lin_attn_fwd": (ctypes.c_int, [_DP, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
     "cp_ulysses_attn_bwd": (ctypes.c_int, [_DP, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
+    "cp_ring_attn_fwd": (ctypes.c_int, [_DP, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P, _P]),
+    "cp_set_debug_checks": (ctypes.c_int, [ctypes.c_int32, ctypes.POINTER(ctypes.c_int32)]),
 }
 for _name, (_res, _args) in _sigs.items():
     _f = getattr(_lib, _name)
@@ -272,6 +275,27 @@ def cp_attn_bwd(prob: Problem, q, k, v, o, lse, dout, dq=None, dk=None, dv=None,
     return dq, dk, dv
 
 
+def cp_ring_attn_fwd(prob: Problem, q, k, v, o=None, lse=None, ws=None, stream=None, comm_stream=None,
+                     overlap: bool = True):
+    """Ring forward with explicit KV transport: C steps, each rank's block
+    against the shard it holds, while the shards move one rank on through
+    device-to-device copies on ``comm_stream`` (a new stream when None and
+    ``overlap``; ``overlap=False`` serialises the copies on ``stream``)."""
+    d = prob.desc
+    if o is None:
+        o = torch.empty(d.total_tokens, d.hq, d.d_v, dtype=q.dtype, device=q.device)
+    if lse is None:
+        lse = torch.empty(d.hq, d.total_tokens, dtype=torch.float32, device=q.device)
+    if ws is None:
+        ws = workspace(prob, CP_OP_RING_FWD, q.device)
+    if overlap and comm_stream is None:
+        comm_stream = torch.cuda.Stream(device=q.device)
+    xs = _stream(comm_stream) if overlap else None
+    _check(_lib.cp_ring_attn_fwd(prob.ptr, _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(ws), ws.numel(),
+                                 _stream(stream), xs), "cp_ring_attn_fwd")
+    return o, lse
+
+
 def cp_ulysses_a2a(prob: Problem, x: torch.Tensor, inverse: bool = False, out: Optional[torch.Tensor] = None,
                    ws: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
     """Ulysses all-to-all re-layout.  Forward: x [T, H, ...] in sharded order
@@ -376,6 +400,13 @@ def cp_attn_fwd_noalloc(prob: Problem, q, k, v, o, lse, stream=None):
 
 
 NOALLOC_SCRATCH_BYTES = 4 << 20
+
+
+def cp_set_debug_checks(on: bool) -> bool:
+    """Turns the plan checks on or off for later calls; returns the former setting."""
+    prev = ctypes.c_int32(0)
+    _check(_lib.cp_set_debug_checks(int(bool(on)), ctypes.byref(prev)), "cp_set_debug_checks")
+    return bool(prev.value)
 
 
 def cp_device_status(stream=None) -> int:

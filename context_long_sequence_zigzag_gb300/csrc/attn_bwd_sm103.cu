@@ -51,6 +51,7 @@
 #include <cuda_bf16.h>
 
 #include "internal.h"
+#include "plan_check.cuh"
 #include "sm103_ptx.cuh"
 
 namespace cpattn {
@@ -278,6 +279,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dkdv_kernel(const __grid
   }
   const int tile_idx = blockIdx.x / a.hkv;
   const int kvh = blockIdx.x - tile_idx * a.hkv;
+  if (a.debug && !debug_plan_ok(a, tile_idx, kvh, kvh, true, p.err)) return;
   const TileDesc tile = a.tiles[tile_idx];
   const int G = a.hq / a.hkv;
   const int n_steps = (BNQ == 128 ? tile.work : count_steps<BNQ>(a.ranges, tile.range_begin, tile.range_count)) * G;
@@ -629,6 +631,7 @@ __global__ void __launch_bounds__(kThreadsDq, 1) attn_bwd_dq_kernel(const __grid
   const int tile_idx = blockIdx.x / a.hq;
   const int h = head_of_slot(blockIdx.x - tile_idx * a.hq, a);
   const int kvh = a.gqa_interleaved ? h % a.hkv : h / (a.hq / a.hkv);
+  if (a.debug && !debug_plan_ok(a, tile_idx, h, kvh, false, p.err)) return;
   const TileDesc tile = a.tiles[tile_idx];
   const int n_kv = tile.work;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;

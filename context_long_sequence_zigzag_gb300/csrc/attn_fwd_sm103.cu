@@ -39,6 +39,7 @@
 #include <cuda_bf16.h>
 
 #include "internal.h"
+#include "plan_check.cuh"
 #include "sm103_ptx.cuh"
 
 namespace cpattn {
@@ -50,7 +51,8 @@ constexpr int BN = 128;  // key rows per step
 constexpr uint32_t kSubTile = 128 * 128;  // one 128-row x 64-column bf16 swizzle panel: 16 KiB
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
-constexpr float kRescaleThreshold = 8.0f;  // log2 units: P stays below 2^8
+constexpr float kRescaleThreshold = 8.0f;  // log2 units: a new maximum moves the reference past this
+constexpr float kLagSum = 1.0995116e12f;    // 2^40: a tile's row sum above this sends it down the full path
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 
 enum WaitSite : int {
@@ -133,6 +135,7 @@ __global__ void __launch_bounds__(224, 1) attn_fwd_tc_kernel(const __grid_consta
   const int tile_idx = blockIdx.x / a.hq;
   const int h = head_of_slot(blockIdx.x - tile_idx * a.hq, a);
   const int kvh = a.gqa_interleaved ? h % a.hkv : h / (a.hq / a.hkv);
+  if (a.debug && !debug_plan_ok(a, tile_idx, h, kvh, false, p.err)) return;
   const TileDesc tile = a.tiles[tile_idx];
   const int n_kv = tile.work;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -291,7 +294,9 @@ __global__ void __launch_bounds__(224, 1) attn_fwd_tc_kernel(const __grid_consta
     const int qpos = tile.pos0 + row;
     const bool row_ok = row < tile.nrows;
     const int64_t qrow = int64_t(tile.row0) + row;
-    float m_ref = -INFINITY;  // reference maximum of scale*log2e*s (log2 units)
+    // reference maximum of scale*log2e*s (log2 units); rows past the tile use 0
+    // so that they never hold their warp on the full path
+    float m_ref = row_ok ? -INFINITY : 0.f;
     float l = 0.f;
     bool ok = true;
     KvCursor cur;
@@ -315,62 +320,75 @@ __global__ void __launch_bounds__(224, 1) attn_fwd_tc_kernel(const __grid_consta
       const int kn = cur.n(), kp = cur.pos();
       int lim = row_ok ? kn : 0;
       if (a.causal) lim = min(lim, qpos - kp + 1);
-      // row maximum over 8 independent chains (one warp per SMSP: the
-      // latency of a single 128-long dependent chain would dominate)
-      float m8[8];
-#pragma unroll
-      for (int e = 0; e < 8; ++e) m8[e] = -INFINITY;
       if (lim < BN) {
 #pragma unroll
         for (int c = 0; c < 4; ++c)
 #pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            const float s = c * 32 + i < lim ? __uint_as_float(sr[c][i]) : -INFINITY;
-            sr[c][i] = __float_as_uint(s);
-            m8[i & 7] = fmaxf(m8[i & 7], s);
+          for (int i = 0; i < 32; ++i)
+            if (c * 32 + i >= lim) sr[c][i] = __float_as_uint(-INFINITY);
+      }
+      // P = exp2(s * scale * log2e - mref) (bf16, two per column) over the
+      // first half of the S buffer (PV(j-3) finished reading it before S(j)
+      // was issued); returns the row sum, kept in 8 chains as 4 packed pairs
+      const uint64_t sl2x2 = ptx::f32x2(sl2, sl2);
+      auto exp_tile = [&](float mref) {
+        uint64_t r2[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) r2[e] = 0ull;
+        const uint64_t nmx2 = ptx::f32x2(-mref, -mref);
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const uint64_t x = ptx::fma_f32x2(
+                ptx::f32x2(__uint_as_float(sr[c][2 * i]), __uint_as_float(sr[c][2 * i + 1])), sl2x2, nmx2);
+            float x0, x1;
+            ptx::f32x2_split(x, x0, x1);
+            const float e0 = ptx::ex2(x0), e1 = ptx::ex2(x1);
+            r2[i & 3] = ptx::add_f32x2(r2[i & 3], ptx::f32x2(e0, e1));
+            pk[i] = ptx::pack_bf16(e0, e1);
           }
-      } else {
+          ptx::tmem_st16(tS + c * 16, pk);
+        }
+        float r8[8];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) ptx::f32x2_split(r2[e], r8[2 * e], r8[2 * e + 1]);
+        return ((r8[0] + r8[1]) + (r8[2] + r8[3])) + ((r8[4] + r8[5]) + (r8[6] + r8[7]));
+      };
+      // Fast path: exponentiate against the reference maximum as it stands,
+      // without this tile's row maximum.  Exact as long as nothing overflows:
+      // P and the fp32 sums only need the reference within 2^kLagLimit of
+      // the true maximum, which the tile's row sum shows (any element above
+      // 2^kLagLimit makes it exceed that; an overflow makes it inf).  A warp
+      // with a row past that bound, or without a reference yet, takes the
+      // full path: row maximum, rescale when it grew by more than 2^8, and
+      // the exponentials again (overwriting the P just stored).
+      float alpha = 1.f, rs = 0.f;
+      bool full = !__all_sync(0xffffffffu, m_ref != -INFINITY);
+      if (!full) {
+        rs = exp_tile(m_ref);
+        full = __any_sync(0xffffffffu, !(rs <= kLagSum));
+      }
+      if (full) {
+        // row maximum over 8 independent chains (one warp per SMSP: the
+        // latency of a single 128-long dependent chain would dominate)
+        float m8[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) m8[e] = -INFINITY;
 #pragma unroll
         for (int c = 0; c < 4; ++c)
 #pragma unroll
           for (int i = 0; i < 32; ++i) m8[i & 7] = fmaxf(m8[i & 7], __uint_as_float(sr[c][i]));
-      }
-      const float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
-                             fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
-      const float m_new = mx * sl2;
-      float alpha = 1.f;
-      if (m_new > m_ref + kRescaleThreshold) {
-        alpha = ptx::ex2(m_ref - m_new);  // 0 when m_ref = -inf
-        m_ref = m_new;
-      }
-      const float mref = m_ref == -INFINITY ? 0.f : m_ref;
-      // row sum in 8 chains, as 4 packed pairs
-      uint64_t r2[4];
-#pragma unroll
-      for (int e = 0; e < 4; ++e) r2[e] = 0ull;
-      const uint64_t sl2x2 = ptx::f32x2(sl2, sl2), nmx2 = ptx::f32x2(-mref, -mref);
-      // P = exp2(s * scale * log2e - m_ref) (bf16, two per column) over the
-      // first half of the S buffer; PV(j-3) finished reading it before S(j)
-      // was issued
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t pk[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const uint64_t x = ptx::fma_f32x2(
-              ptx::f32x2(__uint_as_float(sr[c][2 * i]), __uint_as_float(sr[c][2 * i + 1])), sl2x2, nmx2);
-          float x0, x1;
-          ptx::f32x2_split(x, x0, x1);
-          const float e0 = ptx::ex2(x0), e1 = ptx::ex2(x1);
-          r2[i & 3] = ptx::add_f32x2(r2[i & 3], ptx::f32x2(e0, e1));
-          pk[i] = ptx::pack_bf16(e0, e1);
+        const float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
+                               fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
+        const float m_new = mx * sl2;
+        if (m_new > m_ref + kRescaleThreshold) {
+          alpha = ptx::ex2(m_ref - m_new);  // 0 when m_ref = -inf
+          m_ref = m_new;
         }
-        ptx::tmem_st16(tS + c * 16, pk);
+        rs = exp_tile(m_ref == -INFINITY ? 0.f : m_ref);
       }
-      float r8[8];
-#pragma unroll
-      for (int e = 0; e < 4; ++e) ptx::f32x2_split(r2[e], r8[2 * e], r8[2 * e + 1]);
-      const float rs = ((r8[0] + r8[1]) + (r8[2] + r8[3])) + ((r8[4] + r8[5]) + (r8[6] + r8[7]));
       l = l * alpha + rs;
       // O may be rescaled once PV(j-1) is complete (rare: the reference
       // maximum only moves when a row's maximum grows by more than 2^8)
@@ -407,7 +425,26 @@ __global__ void __launch_bounds__(224, 1) attn_fwd_tc_kernel(const __grid_consta
     if (ok) {
       ptx::tc_fence_after();
       const float inv = l > 0.f ? 1.f / l : 0.f;
+      const float lse_blk = l > 0.f ? m_ref * kLn2 + logf(l) : -INFINITY;
       const int64_t orow = a.block_mode ? int64_t(tile.out_row0) + row : qrow;
+      // block_mode 2: exact merge of this block's partial (o * inv, lse_blk)
+      // into the accumulator ("Ulysses与Ring-Attention详解" §4.2):
+      // lse = max + log1p(exp(-|a - b|)), o = e^(a - lse) o_acc + e^(b - lse) o;
+      // -inf is the identity on either side.
+      float wa = 0.f, wb = inv, lse_out = lse_blk;
+      if (a.block_mode == 2 && row_ok) {
+        const float la = a.lse[int64_t(h) * a.lse_stride + orow];
+        const float mm = fmaxf(la, lse_blk);
+        if (mm == -INFINITY) {
+          wa = 1.f;
+          wb = 0.f;
+          lse_out = -INFINITY;
+        } else {
+          lse_out = mm + log1pf(expf(-fabsf(la - lse_blk)));
+          wa = expf(la - lse_out);
+          wb = expf(lse_blk - lse_out) * inv;
+        }
+      }
 #pragma unroll 1
       for (int c = 0; c < DV / 32; ++c) {
         uint32_t o[32];
@@ -420,7 +457,16 @@ __global__ void __launch_bounds__(224, 1) attn_fwd_tc_kernel(const __grid_consta
           for (int i = 0; i < 32; ++i) o[i] = 0u;
         }
         if (row_ok) {
-          if (a.block_mode) {
+          if (a.block_mode == 2) {
+            float4* dst = reinterpret_cast<float4*>(static_cast<float*>(a.out) + (orow * a.hq + h) * DV + c * 32);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              const float4 x = dst[i];
+              dst[i] = make_float4(wa * x.x + wb * __uint_as_float(o[4 * i]), wa * x.y + wb * __uint_as_float(o[4 * i + 1]),
+                                   wa * x.z + wb * __uint_as_float(o[4 * i + 2]),
+                                   wa * x.w + wb * __uint_as_float(o[4 * i + 3]));
+            }
+          } else if (a.block_mode) {
             float4* dst = reinterpret_cast<float4*>(static_cast<float*>(a.out) + (orow * a.hq + h) * DV + c * 32);
 #pragma unroll
             for (int i = 0; i < 8; ++i)
@@ -440,7 +486,7 @@ __global__ void __launch_bounds__(224, 1) attn_fwd_tc_kernel(const __grid_consta
           }
         }
       }
-      if (row_ok) a.lse[int64_t(h) * a.lse_stride + orow] = l > 0.f ? m_ref * kLn2 + logf(l) : -INFINITY;
+      if (row_ok) a.lse[int64_t(h) * a.lse_stride + orow] = lse_out;
     }
   }
 
@@ -495,9 +541,9 @@ static cudaError_t launch_fwd_impl(const AttnArgs& a, cudaStream_t st) {
   p.err = device_error_word();
   if (!make_map_3d(&p.tq, a.q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, DQK, a.hq, a.T, 64, BM,
                    CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !make_map_3d(&p.tk, a.k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, DQK, a.hkv, a.T, 64, BN,
+      !make_map_3d(&p.tk, a.k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, DQK, a.hkv, a.T_kv ? a.T_kv : a.T, 64, BN,
                    CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !make_map_3d(&p.tv, a.v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, DV, a.hkv, a.T, 64, BN,
+      !make_map_3d(&p.tv, a.v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, DV, a.hkv, a.T_kv ? a.T_kv : a.T, 64, BN,
                    CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
   cudaError_t e = cudaFuncSetAttribute(attn_fwd_tc_kernel<DQK, DV>, cudaFuncAttributeMaxDynamicSharedMemorySize,

@@ -10,12 +10,14 @@
 //   cut into CP pieces), and "LLM context parallel production guide",
 //   "因果 Attention 会制造 Rank 负载不均" (blocks above the diagonal skipped).
 #include <algorithm>
+#include <atomic>
 #include <cmath>
 #include <cstring>
 #include <mutex>
 #include <vector>
 
 #include "internal.h"
+#include "plan_check.cuh"
 
 namespace cpattn {
 namespace {
@@ -161,8 +163,13 @@ int32_t ceil_tiles(int64_t n) { return int32_t((n + kTile - 1) / kTile); }
 
 // Query-major plan: every query tile with the key runs it must visit, in ring
 // order r, r-1, ..., r-C+1 (mod C).  q_rank / kv_rank >= 0 restrict the plan
-// to one (query shard, key shard) block.
-Plan build_fwd_plan(const cp_desc_t* d, const ShardMap& m, int q_rank, int kv_rank) {
+// to one (query shard, key shard) block.  ring_step >= 0 gives one step of
+// the transported ring instead: every rank's query tiles against the shard
+// it holds at that step, rho = (r - step) mod C; from step 1 on that shard
+// sits in the holder's slot of a ring buffer whose rank slots are slot_rows
+// rows apart, and tiles that see nothing of it are left out.
+Plan build_fwd_plan(const cp_desc_t* d, const ShardMap& m, int q_rank, int kv_rank, int ring_step = -1,
+                    int64_t slot_rows = 0) {
   Plan p;
   const bool causal = d->causal != 0;
   for (const Chunk& A : m.chunks) {
@@ -180,12 +187,13 @@ Plan build_fwd_plan(const cp_desc_t* d, const ShardMap& m, int q_rank, int kv_ra
       for (int step = 0; step < m.C; ++step) {
         const int rho = ((A.rank - step) % m.C + m.C) % m.C;
         if (kv_rank >= 0 && rho != kv_rank) continue;
+        if (ring_step >= 0 && step != ring_step) continue;
         for (int k = 0; k < m.per; ++k) {
           const Chunk& B = m.at(rho, A.seq, k);
           if (B.len == 0) continue;
           RangeDesc r{};
           const int32_t bpos = key_pos0(m, B, A);
-          r.row0 = int32_t(B.srow0);
+          r.row0 = ring_step > 0 ? int32_t(A.rank * slot_rows + (B.srow0 - m.rank_off[rho])) : int32_t(B.srow0);
           r.pos0 = bpos;
           if (causal) {
             if (bpos > qmax) continue;  // entirely in the future: skipped
@@ -201,6 +209,7 @@ Plan build_fwd_plan(const cp_desc_t* d, const ShardMap& m, int q_rank, int kv_ra
       }
       t.range_count = int32_t(p.ranges.size()) - t.range_begin;
       t.work = work;
+      if (ring_step > 0 && t.range_count == 0) continue;  // merging nothing would leave the accumulator as is
       p.max_ranges = std::max(p.max_ranges, t.range_count);
       p.tiles.push_back(t);
     }
@@ -291,6 +300,29 @@ cudaError_t upload_plan(const Plan& p, char* base, cudaStream_t st, const TileDe
   return cudaSuccess;
 }
 
+// Debug checks (cp_set_debug_checks): process-wide, read when a call starts.
+std::atomic<int32_t> g_debug_checks{0};
+
+// Uploads a plan into the workspace at `base` and points the kernel
+// arguments at it.  With debug checks on, every entry is first checked on
+// the host against the rows its tensors have (tile_rows for the tiles,
+// range_rows for the runs); an inconsistent plan is refused before any GPU
+// work of the call.
+cp_status_t stage_plan(const Plan& p, char* base, cudaStream_t st, AttnArgs& a, int64_t tile_rows,
+                       int64_t range_rows) {
+  if (a.debug) {
+    for (int32_t i = 0; i < int32_t(p.tiles.size()); ++i)
+      if (plan_entry_check(p.tiles.data(), int32_t(p.tiles.size()), p.ranges.data(), int32_t(p.ranges.size()), i, 0,
+                           1, 0, 1, tile_rows, range_rows, a.block_mode, a.lse_stride) != 0)
+        return CP_ERR_INVALID_ARG;
+  }
+  if (upload_plan(p, base, st, &a.tiles, &a.ranges) != cudaSuccess) return CP_ERR_CUDA;
+  a.num_tiles = int32_t(p.tiles.size());
+  a.num_ranges = int32_t(p.ranges.size());
+  a.max_ranges = p.max_ranges;
+  return CP_OK;
+}
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
 
 bool use_tc_fwd(const cp_desc_t* d) {
@@ -311,6 +343,7 @@ AttnArgs base_args(const cp_desc_t* d) {
   a.gqa_interleaved = d->gqa == CP_GQA_INTERLEAVED;
   a.causal = d->causal;
   a.scale = d->scale;
+  a.debug = g_debug_checks.load();
   return a;
 }
 
@@ -320,9 +353,8 @@ cp_status_t run_bwd_dkdv(const cp_desc_t* d, const ShardMap& m, AttnArgs a, char
   Plan pb = build_bwd_plan(d, m);
   order_by_work(pb);
   if (ws == nullptr || (reinterpret_cast<uintptr_t>(ws) & 255) || ws_bytes < plan_bytes(pb)) return CP_ERR_WORKSPACE;
-  if (upload_plan(pb, ws, cs, &a.tiles, &a.ranges) != cudaSuccess) return CP_ERR_CUDA;
-  a.num_tiles = int32_t(pb.tiles.size());
-  a.max_ranges = pb.max_ranges;
+  const cp_status_t st = stage_plan(pb, ws, cs, a, d->total_tokens, d->total_tokens);
+  if (st != CP_OK) return st;
   const cudaError_t e = use_tc_bwd(d) ? launch_tc_bwd_dkdv(a, cs) : launch_simt_bwd_dkdv(a, d->dtype, cs);
   return e == cudaSuccess ? CP_OK : CP_ERR_CUDA;
 }
@@ -333,9 +365,8 @@ cp_status_t run_bwd_dq(const cp_desc_t* d, const ShardMap& m, AttnArgs a, char* 
   Plan pf = build_fwd_plan(d, m, -1, -1);
   order_by_work(pf);
   if (ws == nullptr || (reinterpret_cast<uintptr_t>(ws) & 255) || ws_bytes < plan_bytes(pf)) return CP_ERR_WORKSPACE;
-  if (upload_plan(pf, ws, cs, &a.tiles, &a.ranges) != cudaSuccess) return CP_ERR_CUDA;
-  a.num_tiles = int32_t(pf.tiles.size());
-  a.max_ranges = pf.max_ranges;
+  const cp_status_t st = stage_plan(pf, ws, cs, a, d->total_tokens, d->total_tokens);
+  if (st != CP_OK) return st;
   const cudaError_t e = use_tc_bwd(d) ? launch_tc_bwd_dq(a, cs) : launch_simt_bwd_dq(a, d->dtype, cs);
   return e == cudaSuccess ? CP_OK : CP_ERR_CUDA;
 }
@@ -495,6 +526,40 @@ BwdLayout bwd_layout(const cp_desc_t* d, const Plan& pf, const Plan& pb) {
   return L;
 }
 
+// ---------------------------------------------------------------- ring with transport
+// Workspace of cp_ring_attn_fwd: the C step plans, two ring buffers of K and
+// V (every rank has a slot of slot_rows rows in each), and the fp32 output
+// accumulator (bf16 problems; fp32 ones accumulate in o itself).
+struct RingLayout {
+  std::vector<Plan> plans;
+  std::vector<size_t> plan_off;
+  int64_t slot_rows = 0;
+  size_t kslot[2] = {0, 0}, vslot[2] = {0, 0}, oacc = 0, total = 0;
+};
+RingLayout ring_layout(const cp_desc_t* d, const ShardMap& m) {
+  RingLayout L;
+  for (int r = 0; r < m.C; ++r) L.slot_rows = std::max<int64_t>(L.slot_rows, m.rank_off[r + 1] - m.rank_off[r]);
+  size_t off = 0;
+  for (int s = 0; s < m.C; ++s) {
+    L.plans.push_back(build_fwd_plan(d, m, -1, -1, s, L.slot_rows));
+    order_by_work(L.plans.back());
+    L.plan_off.push_back(off);
+    off += plan_bytes(L.plans.back());
+  }
+  const size_t elt = d->dtype == CP_DT_BF16 ? 2 : 4;
+  const size_t slot_rows = size_t(m.C) * size_t(L.slot_rows);
+  for (int b = 0; b < 2; ++b) {
+    L.kslot[b] = off;
+    off += align256(slot_rows * d->hkv * d->d_qk * elt);
+    L.vslot[b] = off;
+    off += align256(slot_rows * d->hkv * d->d_v * elt);
+  }
+  L.oacc = off;
+  if (d->dtype == CP_DT_BF16) off += align256(size_t(d->total_tokens) * d->hq * d->d_v * 4);
+  L.total = off;
+  return L;
+}
+
 }  // namespace
 }  // namespace cpattn
 
@@ -588,6 +653,8 @@ cp_status_t cp_workspace_size(const cp_desc_t* d, int32_t op, size_t* bytes) {
     *bytes = plan_bytes(build_bwd_plan(d, m));
   } else if (op == CP_OP_BWD_DQ) {
     *bytes = plan_bytes(build_fwd_plan(d, m, -1, -1));
+  } else if (op == CP_OP_RING_FWD) {
+    *bytes = ring_layout(d, m).total;
   } else if (op == CP_OP_ULYSSES_FWD || op == CP_OP_ULYSSES_BWD) {
     st = check_ulysses(d);
     if (st != CP_OK) return st;
@@ -701,9 +768,6 @@ cp_status_t cp_attn_block_fwd(const cp_desc_t* d, int32_t q_rank, int32_t kv_ran
     return CP_ERR_WORKSPACE;
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
   AttnArgs a = base_args(d);
-  if (upload_plan(p, static_cast<char*>(ws), cs, &a.tiles, &a.ranges) != cudaSuccess) return CP_ERR_CUDA;
-  a.num_tiles = int32_t(p.tiles.size());
-  a.max_ranges = p.max_ranges;
   a.q = q;
   a.k = k;
   a.v = v;
@@ -711,6 +775,8 @@ cp_status_t cp_attn_block_fwd(const cp_desc_t* d, int32_t q_rank, int32_t kv_ran
   a.lse = lse_part;
   a.lse_stride = Tr;
   a.block_mode = 1;
+  st = stage_plan(p, static_cast<char*>(ws), cs, a, d->total_tokens, d->total_tokens);
+  if (st != CP_OK) return st;
   cudaError_t e = use_tc_fwd(d) ? launch_tc_fwd(a, cs) : launch_simt_fwd(a, d->dtype, cs);
   return e == cudaSuccess ? CP_OK : CP_ERR_CUDA;
 }
@@ -730,9 +796,8 @@ cp_status_t cp_attn_fwd(const cp_desc_t* d, const void* q, const void* k, const 
     return CP_ERR_WORKSPACE;
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
   AttnArgs a = base_args(d);
-  if (upload_plan(p, static_cast<char*>(ws), cs, &a.tiles, &a.ranges) != cudaSuccess) return CP_ERR_CUDA;
-  a.num_tiles = int32_t(p.tiles.size());
-  a.max_ranges = p.max_ranges;
+  st = stage_plan(p, static_cast<char*>(ws), cs, a, d->total_tokens, d->total_tokens);
+  if (st != CP_OK) return st;
   a.q = q;
   a.k = k;
   a.v = v;
@@ -832,9 +897,8 @@ cp_status_t cp_attn_fwd_noalloc(const cp_desc_t* d, const void* q, const void* k
   if (noalloc_scratch(&scratch) != cudaSuccess) return CP_ERR_CUDA;
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
   AttnArgs a = base_args(d);
-  if (upload_plan(p, static_cast<char*>(scratch), cs, &a.tiles, &a.ranges) != cudaSuccess) return CP_ERR_CUDA;
-  a.num_tiles = int32_t(p.tiles.size());
-  a.max_ranges = p.max_ranges;
+  st = stage_plan(p, static_cast<char*>(scratch), cs, a, d->total_tokens, d->total_tokens);
+  if (st != CP_OK) return st;
   a.q = q;
   a.k = k;
   a.v = v;
@@ -842,6 +906,92 @@ cp_status_t cp_attn_fwd_noalloc(const cp_desc_t* d, const void* q, const void* k
   a.lse = lse;
   cudaError_t e = use_tc_fwd(d) ? launch_tc_fwd(a, cs) : launch_simt_fwd(a, d->dtype, cs);
   return e == cudaSuccess ? CP_OK : CP_ERR_CUDA;
+}
+
+cp_status_t cp_ring_attn_fwd(const cp_desc_t* d, const void* q, const void* k, const void* v, void* o, float* lse,
+                             void* ws, size_t ws_bytes, cp_stream_t stream, cp_stream_t comm_stream) {
+  cp_status_t st = check_attn_fields(d);
+  if (st != CP_OK) return st;
+  if (d->total_tokens == 0) return CP_OK;
+  const void* ptrs[] = {q, k, v, o, lse};
+  for (const void* p : ptrs)
+    if (p == nullptr || !aligned16(p)) return CP_ERR_INVALID_ARG;
+  const ShardMap m = build_map(d);
+  const RingLayout L = ring_layout(d, m);
+  if (ws == nullptr || (reinterpret_cast<uintptr_t>(ws) & 255) || ws_bytes < L.total) return CP_ERR_WORKSPACE;
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  cudaStream_t xs = comm_stream ? reinterpret_cast<cudaStream_t>(comm_stream) : cs;
+  char* base = static_cast<char*>(ws);
+  const size_t elt = d->dtype == CP_DT_BF16 ? 2 : 4;
+  const size_t krow = size_t(d->hkv) * d->d_qk * elt, vrow = size_t(d->hkv) * d->d_v * elt;
+  const bool tc = use_tc_fwd(d);
+  float* oacc = d->dtype == CP_DT_BF16 ? reinterpret_cast<float*>(base + L.oacc) : static_cast<float*>(o);
+
+  std::vector<AttnArgs> args(m.C);
+  for (int s = 0; s < m.C; ++s) {
+    AttnArgs& a = args[s];
+    a = base_args(d);
+    a.q = q;
+    a.k = s == 0 ? k : base + L.kslot[s % 2];
+    a.v = s == 0 ? v : base + L.vslot[s % 2];
+    a.T_kv = s == 0 ? 0 : int64_t(m.C) * L.slot_rows;
+    a.out = oacc;
+    a.lse = lse;
+    a.lse_stride = d->total_tokens;
+    a.block_mode = s == 0 ? 1 : 2;
+    st = stage_plan(L.plans[s], base + L.plan_off[s], cs, a, d->total_tokens, a.T_kv ? a.T_kv : d->total_tokens);
+    if (st != CP_OK) return st;
+  }
+  cudaEvent_t ev_comp = nullptr, ev_comm = nullptr;
+  auto cleanup = [&](cp_status_t r) {
+    if (ev_comp) cudaEventDestroy(ev_comp);  // released once the recorded work completes
+    if (ev_comm) cudaEventDestroy(ev_comm);
+    return r;
+  };
+  if (cudaEventCreateWithFlags(&ev_comp, cudaEventDisableTiming) != cudaSuccess ||
+      cudaEventCreateWithFlags(&ev_comm, cudaEventDisableTiming) != cudaSuccess)
+    return cleanup(CP_ERR_CUDA);
+  // A key tile that starts near the end of a shard also loads the slot rows
+  // after it.  Their columns are masked (P = 0), but 0 times a stale NaN
+  // pattern is NaN, so the ring buffers start out zeroed.
+  if (cudaMemsetAsync(base + L.kslot[0], 0, L.oacc - L.kslot[0], cs) != cudaSuccess) return cleanup(CP_ERR_CUDA);
+  // the inputs (and the uploaded plans) are ready on the compute stream
+  if (cudaEventRecord(ev_comp, cs) != cudaSuccess) return cleanup(CP_ERR_CUDA);
+  for (int s = 0; s < m.C; ++s) {
+    // step s reads the slot the transfer of step s-1 filled
+    if (s > 0 && cudaStreamWaitEvent(cs, ev_comm, 0) != cudaSuccess) return cleanup(CP_ERR_CUDA);
+    if (s + 1 < m.C) {
+      // transport for step s+1, overlapping step s: every rank passes the
+      // shard it holds to the next rank.  It overwrites the slots step s-1
+      // read, so it waits for that step.
+      if (cudaStreamWaitEvent(xs, ev_comp, 0) != cudaSuccess) return cleanup(CP_ERR_CUDA);
+      const size_t dst_k = L.kslot[(s + 1) % 2], dst_v = L.vslot[(s + 1) % 2];
+      for (int r = 0; r < m.C; ++r) {
+        const int rho = ((r - s) % m.C + m.C) % m.C;  // the shard rank r holds at step s
+        const int64_t rows = m.rank_off[rho + 1] - m.rank_off[rho];
+        if (rows == 0) continue;
+        const int nxt = (r + 1) % m.C;
+        const char* sk = s == 0 ? static_cast<const char*>(k) + size_t(m.rank_off[r]) * krow
+                                : base + L.kslot[s % 2] + size_t(r) * L.slot_rows * krow;
+        const char* sv = s == 0 ? static_cast<const char*>(v) + size_t(m.rank_off[r]) * vrow
+                                : base + L.vslot[s % 2] + size_t(r) * L.slot_rows * vrow;
+        if (cudaMemcpyAsync(base + dst_k + size_t(nxt) * L.slot_rows * krow, sk, size_t(rows) * krow,
+                            cudaMemcpyDeviceToDevice, xs) != cudaSuccess ||
+            cudaMemcpyAsync(base + dst_v + size_t(nxt) * L.slot_rows * vrow, sv, size_t(rows) * vrow,
+                            cudaMemcpyDeviceToDevice, xs) != cudaSuccess)
+          return cleanup(CP_ERR_CUDA);
+      }
+      if (cudaEventRecord(ev_comm, xs) != cudaSuccess) return cleanup(CP_ERR_CUDA);
+    }
+    // block step s: write (s = 0) or merge into (s > 0) the accumulator
+    const cudaError_t e = tc ? launch_tc_fwd(args[s], cs) : launch_simt_fwd(args[s], d->dtype, cs);
+    if (e != cudaSuccess) return cleanup(CP_ERR_CUDA);
+    if (cudaEventRecord(ev_comp, cs) != cudaSuccess) return cleanup(CP_ERR_CUDA);
+  }
+  if (d->dtype == CP_DT_BF16 &&
+      launch_cast_bf16(oacc, o, d->total_tokens * d->hq * int64_t(d->d_v), cs) != cudaSuccess)
+    return cleanup(CP_ERR_CUDA);
+  return cleanup(CP_OK);
 }
 
 cp_status_t cp_ulysses_a2a(const cp_desc_t* d, const void* in, void* out, int32_t heads, int64_t head_bytes,
@@ -973,6 +1123,13 @@ cp_status_t cp_lin_attn_fwd(const cp_desc_t* d, const void* q, const void* k, co
                          reinterpret_cast<float*>(base + L.init), o, cs) == cudaSuccess
              ? CP_OK
              : CP_ERR_CUDA;
+}
+
+cp_status_t cp_set_debug_checks(int32_t on, int32_t* previous) {
+  if (on != 0 && on != 1) return CP_ERR_INVALID_ARG;
+  const int32_t old = g_debug_checks.exchange(on);
+  if (previous) *previous = old;
+  return CP_OK;
 }
 
 cp_status_t cp_device_status(cp_stream_t stream, int32_t* code) {

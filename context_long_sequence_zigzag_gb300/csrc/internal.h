@@ -70,12 +70,19 @@ struct AttnArgs {
   const TileDesc* tiles;
   const RangeDesc* ranges;
   int32_t num_tiles;
+  int32_t num_ranges;
   int32_t max_ranges;  // longest range list of any tile
+  int32_t debug;       // nonzero: every CTA checks its plan entry first (plan_check.cuh)
+  int32_t* err;        // device error word (set by the launchers)
   int64_t T;
+  int64_t T_kv;        // rows of k / v when they live in their own buffer (0: T)
   int64_t lse_stride;  // T, or the shard's row count in block mode
   int32_t hq, hkv, d_qk, d_v;
   int32_t gqa_interleaved;
   int32_t causal;
+  // 0: o (dtype) and lse of the whole result; 1: fp32 partial o and lse of
+  // one block; 2: merge the block's partial into the fp32 accumulator at
+  // out / lse in place (the ring's per-step update)
   int32_t block_mode;
   float scale;
 };
@@ -116,6 +123,8 @@ cudaError_t launch_ulysses_a2a(const int32_t* perm, int64_t T, int32_t C, int64_
                                void* out, int32_t inverse, cudaStream_t st);
 cudaError_t launch_ulysses_lse(const int32_t* perm, int64_t T, int32_t C, int32_t H, const float* in, float* out,
                                int32_t inverse, cudaStream_t st);
+// o (bf16) = o_acc (fp32) rounded to nearest even, n elements (n % 8 == 0)
+cudaError_t launch_cast_bf16(const float* in, void* out, int64_t n, cudaStream_t st);
 cudaError_t launch_lse_merge(int64_t rows, int32_t hq, int32_t dv, float* o_acc, float* lse_acc,
                              const float* o_part, const float* lse_part, cudaStream_t st);
 cudaError_t launch_simt_fwd(const AttnArgs& a, int32_t dtype, cudaStream_t st);

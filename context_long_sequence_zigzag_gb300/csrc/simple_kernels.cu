@@ -6,6 +6,7 @@
 #include <cmath>
 
 #include "internal.h"
+#include "plan_check.cuh"
 
 namespace cpattn {
 namespace {
@@ -192,6 +193,7 @@ __global__ void __launch_bounds__(256) simt_fwd_kernel(const AttnArgs a) {
   const int tile_idx = blockIdx.x / a.hq;
   const int h = head_of_slot(blockIdx.x - tile_idx * a.hq, a);
   const int kvh = kv_of_head(h, a);
+  if (a.debug && !debug_plan_ok(a, tile_idx, h, kvh, false, a.err)) return;
   const TileDesc t = a.tiles[tile_idx];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const E* q = static_cast<const E*>(a.q);
@@ -234,14 +236,34 @@ __global__ void __launch_bounds__(256) simt_fwd_kernel(const AttnArgs a) {
       }
     }
     const float inv = l > 0.f ? 1.f / l : 0.f;
-    const float lse = l > 0.f ? m + logf(l) : -INFINITY;
+    float lse = l > 0.f ? m + logf(l) : -INFINITY;
     const int64_t orow = a.block_mode ? int64_t(t.out_row0) + r : qrow;
+    // block_mode 2: merge into the fp32 accumulator (the lse merge of
+    // "Ulysses与Ring-Attention详解" §4.2, -inf the identity)
+    float wa = 0.f, wb = inv;
+    if (a.block_mode == 2) {
+      const float la = a.lse[int64_t(h) * a.lse_stride + orow];
+      const float mm = fmaxf(la, lse);
+      if (mm == -INFINITY) {
+        wa = 1.f;
+        wb = 0.f;
+      } else {
+        const float lo = mm + log1pf(expf(-fabsf(la - lse)));
+        wa = expf(la - lo);
+        wb = expf(lse - lo) * inv;
+        lse = lo;
+      }
+      __syncwarp();  // every lane has read the old lse before lane 0 overwrites it
+    }
 #pragma unroll
     for (int e = 0; e < kMaxPerLane; ++e) {
       const int c = lane + 32 * e;
       if (c < a.d_v) {
-        if (a.block_mode)
-          static_cast<float*>(a.out)[(orow * a.hq + h) * a.d_v + c] = acc[e] * inv;
+        float* of = static_cast<float*>(a.out) + (orow * a.hq + h) * a.d_v + c;
+        if (a.block_mode == 2)
+          *of = wa * *of + wb * acc[e];
+        else if (a.block_mode)
+          *of = acc[e] * inv;
         else
           stf(static_cast<E*>(a.out) + (orow * a.hq + h) * a.d_v + c, acc[e] * inv);
       }
@@ -276,6 +298,7 @@ __global__ void __launch_bounds__(256) simt_bwd_dq_kernel(const AttnArgs a) {
   const int tile_idx = blockIdx.x / a.hq;
   const int h = head_of_slot(blockIdx.x - tile_idx * a.hq, a);
   const int kvh = kv_of_head(h, a);
+  if (a.debug && !debug_plan_ok(a, tile_idx, h, kvh, false, a.err)) return;
   const TileDesc t = a.tiles[tile_idx];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const E* q = static_cast<const E*>(a.q);
@@ -334,6 +357,7 @@ __global__ void __launch_bounds__(256) simt_bwd_dkdv_kernel(const AttnArgs a) {
   const int tile_idx = blockIdx.x / a.hkv;
   const int kvh = blockIdx.x - tile_idx * a.hkv;
   const int G = a.hq / a.hkv;
+  if (a.debug && !debug_plan_ok(a, tile_idx, kvh, kvh, true, a.err)) return;
   const TileDesc t = a.tiles[tile_idx];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const E* q = static_cast<const E*>(a.q);
@@ -428,6 +452,33 @@ cudaError_t launch_ulysses_lse(const int32_t* perm, int64_t T, int32_t C, int32_
   return cudaGetLastError();
 }
 
+// fp32 -> bf16 (round to nearest even), 8 elements per thread and step.
+__global__ void __launch_bounds__(256) cast_bf16_kernel(const float4* __restrict__ in, uint4* __restrict__ out,
+                                                        int64_t n8) {
+  for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < n8; i += int64_t(gridDim.x) * blockDim.x) {
+    const float4 x = __ldcs(in + 2 * i), y = __ldcs(in + 2 * i + 1);
+    uint4 r;
+    __nv_bfloat162 b;
+    b = __floats2bfloat162_rn(x.x, x.y);
+    r.x = *reinterpret_cast<uint32_t*>(&b);
+    b = __floats2bfloat162_rn(x.z, x.w);
+    r.y = *reinterpret_cast<uint32_t*>(&b);
+    b = __floats2bfloat162_rn(y.x, y.y);
+    r.z = *reinterpret_cast<uint32_t*>(&b);
+    b = __floats2bfloat162_rn(y.z, y.w);
+    r.w = *reinterpret_cast<uint32_t*>(&b);
+    out[i] = r;
+  }
+}
+
+cudaError_t launch_cast_bf16(const float* in, void* out, int64_t n, cudaStream_t st) {
+  const int64_t n8 = n / 8;
+  if (n8 == 0) return cudaSuccess;
+  const int64_t grid = grid_for(n8, 256);
+  cast_bf16_kernel<<<unsigned(grid), 256, 0, st>>>(reinterpret_cast<const float4*>(in), static_cast<uint4*>(out), n8);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_lse_merge(int64_t rows, int32_t hq, int32_t dv, float* o_acc, float* lse_acc,
                              const float* o_part, const float* lse_part, cudaStream_t st) {
   const int64_t grid = grid_for(rows * hq, 8);
@@ -435,7 +486,9 @@ cudaError_t launch_lse_merge(int64_t rows, int32_t hq, int32_t dv, float* o_acc,
   return cudaGetLastError();
 }
 
-cudaError_t launch_simt_fwd(const AttnArgs& a, int32_t dtype, cudaStream_t st) {
+cudaError_t launch_simt_fwd(const AttnArgs& args, int32_t dtype, cudaStream_t st) {
+  AttnArgs a = args;
+  a.err = device_error_word();
   const int64_t grid = int64_t(a.num_tiles) * a.hq;
   if (grid == 0) return cudaSuccess;
   if (dtype == CP_DT_F32)
@@ -454,7 +507,9 @@ cudaError_t launch_bwd_preprocess(const AttnArgs& a, int32_t dtype, cudaStream_t
   return cudaGetLastError();
 }
 
-cudaError_t launch_simt_bwd_dq(const AttnArgs& a, int32_t dtype, cudaStream_t st) {
+cudaError_t launch_simt_bwd_dq(const AttnArgs& args, int32_t dtype, cudaStream_t st) {
+  AttnArgs a = args;
+  a.err = device_error_word();
   const int64_t grid = int64_t(a.num_tiles) * a.hq;
   if (grid == 0) return cudaSuccess;
   if (dtype == CP_DT_F32)
@@ -464,7 +519,9 @@ cudaError_t launch_simt_bwd_dq(const AttnArgs& a, int32_t dtype, cudaStream_t st
   return cudaGetLastError();
 }
 
-cudaError_t launch_simt_bwd_dkdv(const AttnArgs& a, int32_t dtype, cudaStream_t st) {
+cudaError_t launch_simt_bwd_dkdv(const AttnArgs& args, int32_t dtype, cudaStream_t st) {
+  AttnArgs a = args;
+  a.err = device_error_word();
   const int64_t grid = int64_t(a.num_tiles) * a.hkv;
   if (grid == 0) return cudaSuccess;
   if (dtype == CP_DT_F32)

@@ -89,7 +89,7 @@ typedef enum { CP_DT_F32 = 0, CP_DT_BF16 = 1 } cp_dtype_t;
 typedef enum { CP_GQA_BLOCKED = 0, CP_GQA_INTERLEAVED = 1 } cp_gqa_t;
 typedef enum {
   CP_OP_FWD = 0, CP_OP_BWD = 1, CP_OP_BLOCK_FWD = 2, CP_OP_PERMUTE = 3, CP_OP_BWD_DKDV = 4, CP_OP_BWD_DQ = 5,
-  CP_OP_ULYSSES_A2A = 6, CP_OP_ULYSSES_FWD = 7, CP_OP_ULYSSES_BWD = 8, CP_OP_LIN_FWD = 9
+  CP_OP_ULYSSES_A2A = 6, CP_OP_ULYSSES_FWD = 7, CP_OP_ULYSSES_BWD = 8, CP_OP_LIN_FWD = 9, CP_OP_RING_FWD = 10
 } cp_op_t;
 
 /* Problem descriptor.  Read on the host during each call; not retained. */
@@ -195,6 +195,42 @@ cp_status_t cp_attn_bwd(const cp_desc_t* desc, const void* q, const void* k, con
                         const void* o, const float* lse, const void* dout,
                         void* dq, void* dk, void* dv,
                         void* workspace, size_t workspace_bytes, cp_stream_t stream);
+
+/* Ring attention forward with the KV transport made explicit
+ * ("Ulysses Context Parallelism 的工程取舍全记录" §2: ring attention passes
+ * the KV blocks rank to rank by point-to-point transfers that overlap the
+ * block computation; "LLM context parallel production guide", Ring
+ * Attention: every rank computes its local block while the next KV block is
+ * in flight; "Ulysses与Ring-Attention详解" §4.1-§4.2: each step's (out, lse)
+ * is merged into the running result).
+ * Every virtual rank r owns a receive slot in each of two ring buffers.  In
+ * step s (s = 0 .. C-1) rank r computes its queries against the shard it
+ * holds, rho = (r - s) mod C (its own shard at s = 0, read from k / v; from
+ * s = 1 on the copy in its slot), and merges the block's partial into the
+ * fp32 accumulator in the kernel's epilogue.  Meanwhile, on comm_stream,
+ * every rank sends the shard it holds to rank r + 1 (mod C): one
+ * cudaMemcpyAsync of its K rows and one of its V rows into the other ring
+ * buffer, which is what a point-to-point transfer between two GPUs becomes
+ * when all ranks share one.  Events order the two streams: step s + 1 waits
+ * for the transfer that filled its slots, and that transfer waits for step
+ * s - 1, the last reader of the buffer it overwrites.
+ *   q, k, v    : device, sharded order (as cp_attn_fwd)
+ *   o, lse     : device, as cp_attn_fwd; lse is also the running accumulator
+ *   workspace  : cp_workspace_size(desc, CP_OP_RING_FWD) bytes: the C step
+ *                plans, 2 x 2 ring buffers of C x max_rank_rows rows of K and
+ *                of V, and (bf16 problems) the fp32 o accumulator
+ *                [T, hq, d_v]; fp32 problems accumulate in o itself
+ *   stream     : compute stream; the call's results are complete when the
+ *                work enqueued on it is (the transfers are ordered before the
+ *                last step)
+ *   comm_stream: stream of the transfers; NULL runs them on `stream` too
+ *                (serialised, no overlap)
+ * The result equals cp_attn_fwd's up to the rounding order of the merge.
+ * The call creates two CUDA events and releases them before it returns
+ * (the driver frees them once the enqueued work has used them). */
+cp_status_t cp_ring_attn_fwd(const cp_desc_t* desc, const void* q, const void* k, const void* v,
+                             void* o, float* lse, void* workspace, size_t workspace_bytes,
+                             cp_stream_t stream, cp_stream_t comm_stream);
 
 /* ---------------------------------------------------------------- Ulysses
  * All-to-all ("Ulysses") context parallelism with the C virtual ranks on one
@@ -323,6 +359,19 @@ cp_status_t cp_attn_bwd_dkdv(const cp_desc_t* desc, const void* q, const void* k
 cp_status_t cp_attn_bwd_dq(const cp_desc_t* desc, const void* q, const void* k, const void* v,
                            const float* lse, const float* dpsum, const void* dout, void* dq,
                            void* workspace, size_t workspace_bytes, cp_stream_t stream);
+
+/* Debug checks, process-wide, for the calls that start after this one
+ * (on = 1) or none (on = 0, the default); *previous (may be NULL) receives
+ * the former setting.  With checks on, the host checks every tile plan
+ * against the row counts of the tensors it indexes before uploading it
+ * (CP_ERR_INVALID_ARG if inconsistent), and every CTA of the attention
+ * kernels checks its own plan entry (tile index, heads, tile rows, output
+ * rows, run list and run rows, step count) before any load or store: a bad
+ * entry records 0x200 | check in the device error word (cp_device_status)
+ * and the CTA returns without touching memory.  No check traps.  It stands
+ * in for a memory checker: the pages report a block-write / scalar-read
+ * race that unit tests had missed ("超长上下文训练速度翻倍秘籍" §2). */
+cp_status_t cp_set_debug_checks(int32_t on, int32_t* previous);
 
 /* Synchronises `stream`, then returns and clears the device error word of
  * the current device: *code = 0 when every bounded wait since the last call

@@ -182,3 +182,37 @@ def test_linear_attention_rejected_configurations():
     with pytest.raises(cpa.CpError) as e:
         cpa.cp_workspace_size(cpa.Problem(256, 4, 2, 64, 64, 2, "contiguous"), cpa.CP_OP_LIN_FWD)
     assert e.value.status == cpa.CP_ERR_INVALID_ARG
+
+
+def test_ring_workspace_and_argument_errors():
+    # two ring buffers of K and V with a slot of the longest shard per rank,
+    # plus the fp32 output accumulator of a bf16 problem
+    T, hq, hkv, d, C = 1000, 4, 2, 128, 4
+    p = cpa.Problem(T, hq, hkv, d, d, C, "zigzag", [0, 1000])
+    n = cpa.cp_workspace_size(p, cpa.CP_OP_RING_FWD)
+    slot_rows = max(np.diff(cpa.cp_shard_offsets(p)))
+    assert n >= 2 * C * slot_rows * hkv * 2 * d * 2 + T * hq * d * 4
+    f = cpa.cp_workspace_size(cpa.Problem(T, hq, hkv, d, d, C, "zigzag", [0, 1000], dtype=__import__("torch").float32),
+                              cpa.CP_OP_RING_FWD)
+    assert f < n + 2 * C * slot_rows * hkv * 2 * d * 2  # fp32 accumulates in o: no extra accumulator
+    lib = ctypes.CDLL(cpa.LIB_PATH)
+    fn = lib.cp_ring_attn_fwd
+    fn.restype = ctypes.c_int
+    fn.argtypes = [ctypes.POINTER(cpa.cp_desc_t)] + [ctypes.c_void_p] * 6 + [ctypes.c_size_t] + [ctypes.c_void_p] * 2
+    fake = 1 << 20  # aligned, never dereferenced: both errors are found before any GPU work
+    assert fn(ctypes.byref(p.desc), fake, fake, None, fake, fake, fake, n, None, None) == cpa.CP_ERR_INVALID_ARG
+    assert fn(ctypes.byref(p.desc), fake, fake, fake, fake, fake, fake, n - 1, None, None) == cpa.CP_ERR_WORKSPACE
+    assert fn(ctypes.byref(p.desc), fake, fake, fake, fake, fake, fake + 16, n, None, None) == cpa.CP_ERR_WORKSPACE
+
+
+def test_debug_checks_switch():
+    prev = cpa.cp_set_debug_checks(True)
+    try:
+        assert cpa.cp_set_debug_checks(True) is True
+        assert cpa.cp_set_debug_checks(False) is True
+        assert cpa.cp_set_debug_checks(False) is False
+        lib = ctypes.CDLL(cpa.LIB_PATH)
+        lib.cp_set_debug_checks.argtypes = [ctypes.c_int32, ctypes.c_void_p]
+        assert lib.cp_set_debug_checks(2, None) == cpa.CP_ERR_INVALID_ARG
+    finally:
+        cpa.cp_set_debug_checks(prev)
