@@ -33,6 +33,19 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
+
+def _host_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+# Thread counts of the CPU oracle's BLAS and OpenMP pools, set before numpy
+# and torch load them (an explicit setting from the environment wins).
+for _var in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS"):
+    os.environ.setdefault(_var, str(_host_cores()))
+
 import numpy as np  # noqa: E402
 import torch  # noqa: E402
 
@@ -114,10 +127,22 @@ def recorded_traffic(kernel: str, workload: str):
 
 
 def cpu_cores() -> int:
-    try:
-        return len(os.sched_getaffinity(0))
-    except AttributeError:
-        return os.cpu_count() or 1
+    return _host_cores()
+
+
+def cpu_baseline_entry(w: workloads.Workload, tf: float, secs: float, desc: str) -> dict:
+    """The oracle's measured rate on its sample, the thread counts it ran
+    with, and a labelled extrapolation of that rate to the whole workload
+    (the oracle's cost grows with the visible pairs, as the FLOP count does)."""
+    full = w.flops_fwd() + w.flops_bwd()
+    return {"value": round(tf, 6), "unit": "TFLOP/s", "cores": cpu_cores(), "kind": "oracle", "sample": desc,
+            "seconds": round(secs, 2),
+            "threads": {"OPENBLAS_NUM_THREADS": os.environ.get("OPENBLAS_NUM_THREADS"),
+                        "OMP_NUM_THREADS": os.environ.get("OMP_NUM_THREADS"),
+                        "torch_intraop": torch.get_num_threads()},
+            "extrapolated_full_problem": {"seconds": round(full / (tf * 1e12), 1),
+                                          "note": "estimate: the whole workload's fwd+bwd FLOPs at the sample's "
+                                                  "measured rate; not measured"}}
 
 
 # ----------------------------------------------------------------------------- clocks
@@ -436,14 +461,85 @@ def e2e_measure(r: Runner, steps: int, warmup: int):
                 d2h_done[i].record(s_out)
         comp.wait_stream(s_out)
 
-    pipeline(warmup)
-    torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(comp)
-    pipeline(steps)
-    e1.record(comp)
-    torch.cuda.synchronize()
-    return e0.elapsed_time(e1) / steps, h2d, d2h
+    def serial(n: int):
+        # every copy on the compute stream, in order: nothing overlaps
+        for _ in range(n):
+            for n_, t in host_in.items():
+                r.g[n_].copy_(t, non_blocking=True)
+            r.step(combined_bwd=True)
+            for n_, t in host_out.items():
+                t.copy_(r.out[n_], non_blocking=True)
+
+    def timed(fn, n):
+        fn(warmup)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(comp)
+        fn(n)
+        e1.record(comp)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / n
+
+    ms_pipe = timed(pipeline, steps)
+    ms_serial = timed(serial, max(2, steps // 4))
+    return ms_pipe, ms_serial, h2d, d2h
+
+
+def ring_measure(r: Runner, steps: int = 3, warmup: int = 2) -> dict:
+    """The forward as a ring with explicit KV transport (cp_ring_attn_fwd):
+    C steps of block attention merged into an fp32 accumulator, while every
+    rank's KV shard moves one rank on by device-to-device copies on a second
+    stream.  Device time with the copies on their own stream (overlapped) and
+    serialised on the compute stream, the same set of copies alone, and the
+    share of the copy time the overlap hides."""
+    cpa, w = r.cpa, r.w
+    ws = cpa.workspace(r.prob, cpa.CP_OP_RING_FWD, r.dev)
+    comm = torch.cuda.Stream(priority=-1)  # copies ahead of the attention kernel's waiting CTAs
+    s = r.s
+
+    def timed(overlap: bool) -> float:
+        ev = []
+        for i in range(warmup + steps):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            cpa.cp_ring_attn_fwd(r.prob, s["q"], s["k"], s["v"], r.o, r.lse, ws, comm_stream=comm, overlap=overlap)
+            b.record()
+            if i >= warmup:
+                ev.append((a, b))
+        torch.cuda.synchronize()
+        return statistics.mean(a.elapsed_time(b) for a, b in ev)
+
+    ms_ovl, ms_ser = timed(True), timed(False)
+    status = cpa.cp_device_status()
+    if status != 0:
+        raise RuntimeError(f"device wait timeout code {status:#x} (ring)")
+    # the transfers alone: C - 1 steps, every rank's shard of K and of V
+    off = cpa.cp_shard_offsets(r.prob)
+    C = w.cp_size
+    rows = max(off[i + 1] - off[i] for i in range(C))
+    slot_k = torch.empty(2, C, rows, w.hkv, w.d_qk, dtype=torch.bfloat16, device=r.dev)
+    slot_v = torch.empty(2, C, rows, w.hkv, w.d_v, dtype=torch.bfloat16, device=r.dev)
+    nbytes = 0
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    for rep in range(2):
+        a.record()
+        for st in range(C - 1):
+            for rk in range(C):
+                n = off[(rk - st) % C + 1] - off[(rk - st) % C]
+                dst = (st + 1) % 2
+                slot_k[dst, (rk + 1) % C, :n].copy_(slot_k[st % 2, rk, :n])
+                slot_v[dst, (rk + 1) % C, :n].copy_(slot_v[st % 2, rk, :n])
+                if rep == 0:
+                    nbytes += n * w.hkv * (w.d_qk + w.d_v) * 2
+        b.record()
+        torch.cuda.synchronize()
+    ms_copy = a.elapsed_time(b)
+    del ws, slot_k, slot_v
+    hidden = (ms_ser - ms_ovl) / ms_copy if ms_copy > 0 else 0.0
+    return {"ms_overlapped": round(ms_ovl, 3), "ms_serialised": round(ms_ser, 3), "ms_copies_alone": round(ms_copy, 3),
+            "copy_bytes": nbytes, "hidden_frac_of_copy_time": round(max(0.0, min(1.0, hidden)), 3),
+            "tflops_overlapped": round(w.flops_fwd() / (ms_ovl * 1e-3) / 1e12, 2),
+            "transport": "cudaMemcpyAsync device-to-device, one per rank, K and V, per step; unmeasured across GPUs"}
 
 
 def aux_bandwidth(r: "Runner", reps: int = 5) -> dict:
@@ -544,7 +640,8 @@ def run_gpu(args):
 
     # at least 8 steps: one step's H2D before the first and one D2H after the last are
     # not overlapped, and the per-step number should be the steady state
-    e2e_ms, h2d, d2h = e2e_measure(r, min(max(args.steps, 8), 16), 1)
+    e2e_ms, e2e_serial_ms, h2d, d2h = e2e_measure(r, min(max(args.steps, 8), 16), 1)
+    ring = ring_measure(r) if not args.no_ring else {"skipped": "--no-ring"}
     aux = aux_bandwidth(r)
     uly = ulysses_measure(r) if not args.no_ulysses else {"skipped": "--no-ulysses"}
     lin = linear_measure(dev) if not args.no_linear else {"skipped": "--no-linear"}
@@ -558,13 +655,18 @@ def run_gpu(args):
     value = (f_fwd + f_bwd) * world / (ms * 1e-3) / 1e12
     fwd_tf = f_fwd / (fwd_ms * 1e-3) / 1e12
     bwd_tf = f_bwd / (bwd_ms * 1e-3) / 1e12
-    # work each kernel actually performs (its own GEMMs over visible pairs)
+    # Each kernel is credited only the method's own GEMMs it performs over the
+    # visible pairs: the forward its two (Q K^T, P V); dK/dV four of the
+    # backward's five (Q K^T recomputed, dO V^T, P^T dO, dS^T Q); dQ the fifth
+    # (dS K).  The dQ kernel also recomputes Q K^T and dO V^T, which the
+    # dK/dV kernel already counts: that repeated work is not credited.
     pairs_h = float(w.visible_pairs()) * w.hq
     kernels = {
         "attn_fwd_tc_kernel": (fwd_ms, pairs_h * (2 * w.d_qk + 2 * w.d_v)),
         "attn_bwd_dkdv_kernel": (dkdv_ms, pairs_h * (4 * w.d_qk + 4 * w.d_v)),
-        "attn_bwd_dq_kernel": (dq_ms, pairs_h * (4 * w.d_qk + 2 * w.d_v)),
+        "attn_bwd_dq_kernel": (dq_ms, pairs_h * (2 * w.d_qk)),
     }
+    executed_dq = pairs_h * (4 * w.d_qk + 2 * w.d_v)  # what the dQ kernel runs, recomputation included
     dom = max(kernels, key=lambda k: kernels[k][0])
     dom_ms, dom_flops = kernels[dom]
     dom_tf = dom_flops / (dom_ms * 1e-3) / 1e12
@@ -599,7 +701,13 @@ def run_gpu(args):
                          "kernels": {k: {"ms": round(t, 3), "tflops": round(fl / (t * 1e-3) / 1e12, 2),
                                          "frac": round(fl / (t * 1e-3) / 1e12 / peak_sus, 4),
                                          "frac_of_burst": round(fl / (t * 1e-3) / 1e12 / peak_burst, 4)}
-                                     for k, (t, fl) in kernels.items()}},
+                                     for k, (t, fl) in kernels.items()},
+                         "credit": "method GEMMs only: fwd 2d_qk+2d_v, dK/dV 4d_qk+4d_v, dQ 2d_qk (dS K) per "
+                                   "pair and head",
+                         "dq_kernel_executed_tflops": round(executed_dq / (dq_ms * 1e-3) / 1e12, 2),
+                         "bwd_whole": {"ms": round(bwd_ms, 3), "tflops": round(bwd_tf, 2),
+                                       "frac": round(bwd_tf / peak_sus, 4),
+                                       "frac_of_burst": round(bwd_tf / peak_burst, 4)}},
             "hbm_kernels": {k: dict(v, frac=round(v["gbs"] / float(peaks.get("hbm_gbs", FALLBACK["hbm_gbs"])), 4),
                                     peak_gbs=float(peaks.get("hbm_gbs", FALLBACK["hbm_gbs"])))
                             for k, v in aux.items()},
@@ -608,12 +716,16 @@ def run_gpu(args):
             "e2e": {"value": round((f_fwd + f_bwd) * world / (e2e_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 3),
                     "copies": "pinned host buffers; step i+1's H2D and step i's D2H on two copy streams, "
-                              "overlapping the kernels"},
+                              "overlapping the kernels",
+                    "serialised": {"value": round((f_fwd + f_bwd) * world / (e2e_serial_ms * 1e-3) / 1e12, 2),
+                                   "ms_per_step": round(e2e_serial_ms, 3),
+                                   "copies": "the same copies in order on the compute stream, nothing overlapped"}},
             "clocks": clk,
             "gpu_launches": r.launches_per_step * args.steps,
             "rank_block_counts": cpa.cp_rank_block_counts(r.prob),
             "rank_balance": balance_report(cpa, w),
             "ulysses": uly,
+            "ring_transport": ring,
             "other_configs": others,
             "linear_attention_cp": lin,
         }
@@ -624,8 +736,7 @@ def run_gpu(args):
             uly["a2a_q"]["frac"] = round(uly["a2a_q"]["gbs"] / hbm, 4)
         if not args.no_cpu_baseline:
             tf, secs, desc = oracle_sample(w, args.cpu_tokens)
-            result["cpu_baseline"] = {"value": round(tf, 6), "unit": "TFLOP/s", "cores": cpu_cores(),
-                                      "kind": "oracle", "sample": desc, "seconds": round(secs, 2)}
+            result["cpu_baseline"] = cpu_baseline_entry(w, tf, secs, desc)
     if world > 1:
         torch.distributed.destroy_process_group()
     return result
@@ -667,8 +778,7 @@ def run_reference(args):
         "data": "synthetic (seeded iid N(0,1) q, k, v, dout)",
         "config": {"workload": w.name, "total_tokens": w.total_tokens, "hq": w.hq, "hkv": w.hkv, "d_qk": w.d_qk,
                    "d_v": w.d_v, "cp_size": w.cp_size, "layout": w.layout},
-        "cpu_baseline": {"value": round(v, 6), "unit": "TFLOP/s", "cores": cpu_cores(), "kind": "oracle",
-                         "sample": desc},
+        "cpu_baseline": cpu_baseline_entry(w, v, statistics.mean(secs), desc),
         "e2e": {"value": round(v, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
 
@@ -684,6 +794,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-ulysses", action="store_true", help="skip the Ulysses comparison")
     ap.add_argument("--no-linear", action="store_true", help="skip the linear-attention CP measurement")
+    ap.add_argument("--no-ring", action="store_true", help="skip the ring-with-transport measurement")
     ap.add_argument("--no-other-configs", action="store_true",
                     help="skip the throughput lines of the other standard problems")
     ap.add_argument("--layout", default=None, choices=["contiguous", "zigzag", "striped"],

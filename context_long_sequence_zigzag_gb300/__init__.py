@@ -279,8 +279,10 @@ def cp_ring_attn_fwd(prob: Problem, q, k, v, o=None, lse=None, ws=None, stream=N
                      overlap: bool = True):
     """Ring forward with explicit KV transport: C steps, each rank's block
     against the shard it holds, while the shards move one rank on through
-    device-to-device copies on ``comm_stream`` (a new stream when None and
-    ``overlap``; ``overlap=False`` serialises the copies on ``stream``)."""
+    device-to-device copies on ``comm_stream`` (a new high-priority stream
+    when None and ``overlap``, so that the copies are not queued behind the
+    attention kernel's waiting CTAs; ``overlap=False`` serialises the copies
+    on ``stream``)."""
     d = prob.desc
     if o is None:
         o = torch.empty(d.total_tokens, d.hq, d.d_v, dtype=q.dtype, device=q.device)
@@ -289,7 +291,7 @@ def cp_ring_attn_fwd(prob: Problem, q, k, v, o=None, lse=None, ws=None, stream=N
     if ws is None:
         ws = workspace(prob, CP_OP_RING_FWD, q.device)
     if overlap and comm_stream is None:
-        comm_stream = torch.cuda.Stream(device=q.device)
+        comm_stream = torch.cuda.Stream(device=q.device, priority=-1)
     xs = _stream(comm_stream) if overlap else None
     _check(_lib.cp_ring_attn_fwd(prob.ptr, _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(ws), ws.numel(),
                                  _stream(stream), xs), "cp_ring_attn_fwd")
