@@ -497,7 +497,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dkdv_kernel(const __grid
       const int cmax = (r < nk ? nq : 0) - int(colS);             // columns [cmin, cmax) are visible
 
       // ---- P^T = exp(S^T * scale - lse)
-      if (!__all_sync(0xffffffffu, ptx::mbar_wait(bar_s_full, i & 1, kSiteSFull, wctx))) { ok = false; break; }
+      if (!__all_sync(0xffffffffu, ptx::mbar_wait_poll(bar_s_full, i & 1, kSiteSFull, wctx))) { ok = false; break; }
       ptx::tc_fence_after();
       uint32_t x[NC / 32][32];
       ldcols<NC>(tS + colS, x);
@@ -522,7 +522,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dkdv_kernel(const __grid
       if (lane == 0) ptx::mbar_arrive(bar_p_full);
 
       // ---- dS^T = P^T (dP^T - D) * scale
-      if (!__all_sync(0xffffffffu, ptx::mbar_wait(bar_dp_full, i & 1, kSiteDPFull, wctx))) { ok = false; break; }
+      if (!__all_sync(0xffffffffu, ptx::mbar_wait_poll(bar_dp_full, i & 1, kSiteDPFull, wctx))) { ok = false; break; }
       ptx::tc_fence_after();
       ldcols<NC>(tDP + colS, x);
 #pragma unroll

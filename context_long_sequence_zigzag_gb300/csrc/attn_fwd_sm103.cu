@@ -304,7 +304,7 @@ __global__ void __launch_bounds__(224, 1) attn_fwd_tc_kernel(const __grid_consta
     for (int j = 0; j < n_kv; ++j, cur.next()) {
       const int sb = j % Cfg::NS_S;
       const uint32_t tS = tmem + lane_base + Cfg::tS0 + BN * sb;
-      if (!__all_sync(0xffffffffu, ptx::mbar_wait(bar_s_full(sb), (j / Cfg::NS_S) & 1, kSiteSFull, wctx))) {
+      if (!__all_sync(0xffffffffu, ptx::mbar_wait_poll(bar_s_full(sb), (j / Cfg::NS_S) & 1, kSiteSFull, wctx))) {
         ok = false;
         break;
       }

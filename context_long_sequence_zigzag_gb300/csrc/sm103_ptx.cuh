@@ -54,6 +54,19 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Non-blocking test of the same phase completion.
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 // Shared state of the bounded waits of one CTA: the time limit, the CTA's
 // abort flag (shared memory) and the device error word.
 struct WaitCtx {
@@ -72,6 +85,26 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int sit
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((it & 15u) == 0) {
+      if (*ctx.abort) return false;
+      if (globaltimer() - t0 > ctx.limit_ns) {
+        *ctx.abort = 1;
+        if (ctx.err) atomicCAS(ctx.err, 0, 0x100 | site);
+        return false;
+      }
+    }
+  }
+}
+
+// The same bounded wait by polling with test_wait.  For the compute warps'
+// waits on tensor-core results: try_wait may suspend the thread, and
+// measured on GB300 the forward and the dK/dV kernel run 4-9 % faster when
+// their compute warps poll instead (the warp has nothing else to issue).
+__device__ __forceinline__ bool mbar_wait_poll(uint32_t bar, uint32_t parity, int site, const WaitCtx& ctx) {
+  if (mbar_test_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_test_wait(bar, parity)) return true;
+    if ((it & 255u) == 0) {
       if (*ctx.abort) return false;
       if (globaltimer() - t0 > ctx.limit_ns) {
         *ctx.abort = 1;
