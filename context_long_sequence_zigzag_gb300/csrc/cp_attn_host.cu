@@ -530,11 +530,18 @@ BwdLayout bwd_layout(const cp_desc_t* d, const Plan& pf, const Plan& pb) {
 // Workspace of cp_ring_attn_fwd: the C step plans, two ring buffers of K and
 // V (every rank has a slot of slot_rows rows in each), and the fp32 output
 // accumulator (bf16 problems; fp32 ones accumulate in o itself).
+// The transfers of step s (s = 0 .. C-2) are one copy list per tensor
+// (K, then V): every rank's shard into the next rank's slot.  Offsets are
+// relative to the list's source (k / v at s = 0, else the step's ring
+// buffer) and destination (the other ring buffer).
 struct RingLayout {
   std::vector<Plan> plans;
   std::vector<size_t> plan_off;
+  std::vector<CopySeg> segs;       // all lists, back to back
+  std::vector<int32_t> seg_begin;  // list l = 2 * s + tensor: segs[seg_begin[l] .. seg_begin[l + 1])
+  std::vector<int64_t> pieces;     // 32 KiB pieces of list l
   int64_t slot_rows = 0;
-  size_t kslot[2] = {0, 0}, vslot[2] = {0, 0}, oacc = 0, total = 0;
+  size_t segs_off = 0, kslot[2] = {0, 0}, vslot[2] = {0, 0}, oacc = 0, total = 0;
 };
 RingLayout ring_layout(const cp_desc_t* d, const ShardMap& m) {
   RingLayout L;
@@ -547,6 +554,29 @@ RingLayout ring_layout(const cp_desc_t* d, const ShardMap& m) {
     off += plan_bytes(L.plans.back());
   }
   const size_t elt = d->dtype == CP_DT_BF16 ? 2 : 4;
+  const int64_t row_bytes[2] = {int64_t(d->hkv) * d->d_qk * int64_t(elt), int64_t(d->hkv) * d->d_v * int64_t(elt)};
+  for (int s = 0; s + 1 < m.C; ++s) {
+    for (int t = 0; t < 2; ++t) {
+      L.seg_begin.push_back(int32_t(L.segs.size()));
+      int64_t pieces = 0;
+      for (int r = 0; r < m.C; ++r) {
+        const int rho = ((r - s) % m.C + m.C) % m.C;  // the shard rank r holds at step s
+        const int64_t rows = m.rank_off[rho + 1] - m.rank_off[rho];
+        if (rows == 0) continue;
+        CopySeg g;
+        g.src = (s == 0 ? m.rank_off[r] : r * L.slot_rows) * row_bytes[t];
+        g.dst = int64_t((r + 1) % m.C) * L.slot_rows * row_bytes[t];
+        g.bytes = rows * row_bytes[t];
+        g.piece0 = pieces;
+        pieces += (g.bytes + kPermutePiece - 1) / kPermutePiece;
+        L.segs.push_back(g);
+      }
+      L.pieces.push_back(pieces);
+    }
+  }
+  L.seg_begin.push_back(int32_t(L.segs.size()));
+  L.segs_off = off;
+  off += align256(std::max<size_t>(L.segs.size(), 1) * sizeof(CopySeg));
   const size_t slot_rows = size_t(m.C) * size_t(L.slot_rows);
   for (int b = 0; b < 2; ++b) {
     L.kslot[b] = off;
@@ -922,8 +952,6 @@ cp_status_t cp_ring_attn_fwd(const cp_desc_t* d, const void* q, const void* k, c
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
   cudaStream_t xs = comm_stream ? reinterpret_cast<cudaStream_t>(comm_stream) : cs;
   char* base = static_cast<char*>(ws);
-  const size_t elt = d->dtype == CP_DT_BF16 ? 2 : 4;
-  const size_t krow = size_t(d->hkv) * d->d_qk * elt, vrow = size_t(d->hkv) * d->d_v * elt;
   const bool tc = use_tc_fwd(d);
   float* oacc = d->dtype == CP_DT_BF16 ? reinterpret_cast<float*>(base + L.oacc) : static_cast<float*>(o);
 
@@ -955,6 +983,9 @@ cp_status_t cp_ring_attn_fwd(const cp_desc_t* d, const void* q, const void* k, c
   // after it.  Their columns are masked (P = 0), but 0 times a stale NaN
   // pattern is NaN, so the ring buffers start out zeroed.
   if (cudaMemsetAsync(base + L.kslot[0], 0, L.oacc - L.kslot[0], cs) != cudaSuccess) return cleanup(CP_ERR_CUDA);
+  if (!L.segs.empty() && cudaMemcpyAsync(base + L.segs_off, L.segs.data(), L.segs.size() * sizeof(CopySeg),
+                                         cudaMemcpyHostToDevice, cs) != cudaSuccess)
+    return cleanup(CP_ERR_CUDA);
   // the inputs (and the uploaded plans) are ready on the compute stream
   if (cudaEventRecord(ev_comp, cs) != cudaSuccess) return cleanup(CP_ERR_CUDA);
   for (int s = 0; s < m.C; ++s) {
@@ -964,22 +995,19 @@ cp_status_t cp_ring_attn_fwd(const cp_desc_t* d, const void* q, const void* k, c
       // transport for step s+1, overlapping step s: every rank passes the
       // shard it holds to the next rank.  It overwrites the slots step s-1
       // read, so it waits for that step.
+      // One copy kernel per tensor with one CTA per SM: a device-to-device
+      // cudaMemcpyAsync runs as a kernel too, and if it is enqueued as the
+      // attention kernel starts it takes every SM first; these CTAs fit
+      // beside the attention kernel's and copy while it computes.
       if (cudaStreamWaitEvent(xs, ev_comp, 0) != cudaSuccess) return cleanup(CP_ERR_CUDA);
-      const size_t dst_k = L.kslot[(s + 1) % 2], dst_v = L.vslot[(s + 1) % 2];
-      for (int r = 0; r < m.C; ++r) {
-        const int rho = ((r - s) % m.C + m.C) % m.C;  // the shard rank r holds at step s
-        const int64_t rows = m.rank_off[rho + 1] - m.rank_off[rho];
-        if (rows == 0) continue;
-        const int nxt = (r + 1) % m.C;
-        const char* sk = s == 0 ? static_cast<const char*>(k) + size_t(m.rank_off[r]) * krow
-                                : base + L.kslot[s % 2] + size_t(r) * L.slot_rows * krow;
-        const char* sv = s == 0 ? static_cast<const char*>(v) + size_t(m.rank_off[r]) * vrow
-                                : base + L.vslot[s % 2] + size_t(r) * L.slot_rows * vrow;
-        if (cudaMemcpyAsync(base + dst_k + size_t(nxt) * L.slot_rows * krow, sk, size_t(rows) * krow,
-                            cudaMemcpyDeviceToDevice, xs) != cudaSuccess ||
-            cudaMemcpyAsync(base + dst_v + size_t(nxt) * L.slot_rows * vrow, sv, size_t(rows) * vrow,
-                            cudaMemcpyDeviceToDevice, xs) != cudaSuccess)
-          return cleanup(CP_ERR_CUDA);
+      for (int t = 0; t < 2; ++t) {
+        const int l = 2 * s + t;
+        const int32_t nseg = L.seg_begin[l + 1] - L.seg_begin[l];
+        if (nseg == 0) continue;
+        const void* src = s == 0 ? (t == 0 ? k : v) : base + (t == 0 ? L.kslot[s % 2] : L.vslot[s % 2]);
+        char* dst = base + (t == 0 ? L.kslot[(s + 1) % 2] : L.vslot[(s + 1) % 2]);
+        const CopySeg* segs = reinterpret_cast<const CopySeg*>(base + L.segs_off) + L.seg_begin[l];
+        if (launch_permute(segs, nseg, L.pieces[l], src, dst, xs, 1) != cudaSuccess) return cleanup(CP_ERR_CUDA);
       }
       if (cudaEventRecord(ev_comm, xs) != cudaSuccess) return cleanup(CP_ERR_CUDA);
     }

@@ -94,8 +94,11 @@ enum : int32_t {
 };
 
 // ---- launchers (each returns cudaSuccess or the launch error) ----
+// ctas_per_sm bounds the grid: 32 for a copy that has the GPU to itself; 1
+// for a copy that must run beside a kernel holding every SM (one 256-thread,
+// 40-register CTA fits next to an attention CTA).
 cudaError_t launch_permute(const CopySeg* segs, int32_t nseg, int64_t npieces,
-                           const void* in, void* out, cudaStream_t st);
+                           const void* in, void* out, cudaStream_t st, int32_t ctas_per_sm = 32);
 // Linear attention with AllGather CP: a block of at most kLinBlock tokens of
 // one rank's piece of one sequence; blocks are listed per sequence in order
 // (ranks in order, blocks in order inside a rank).

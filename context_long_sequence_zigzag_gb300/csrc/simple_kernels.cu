@@ -426,10 +426,10 @@ int64_t grid_for(int64_t work_items, int per_block) {
 }  // namespace
 
 cudaError_t launch_permute(const CopySeg* segs, int32_t nseg, int64_t npieces, const void* in,
-                           void* out, cudaStream_t st) {
+                           void* out, cudaStream_t st, int32_t ctas_per_sm) {
   if (npieces == 0) return cudaSuccess;
   int64_t grid = npieces;
-  const int64_t cap = int64_t(sm_count()) * 32;
+  const int64_t cap = int64_t(sm_count()) * ctas_per_sm;
   if (grid > cap) grid = cap;
   permute_kernel<<<unsigned(grid), kPermThreads, 0, st>>>(segs, nseg, npieces,
                                                           static_cast<const char*>(in),

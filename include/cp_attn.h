@@ -208,17 +208,23 @@ cp_status_t cp_attn_bwd(const cp_desc_t* desc, const void* q, const void* k, con
  * holds, rho = (r - s) mod C (its own shard at s = 0, read from k / v; from
  * s = 1 on the copy in its slot), and merges the block's partial into the
  * fp32 accumulator in the kernel's epilogue.  Meanwhile, on comm_stream,
- * every rank sends the shard it holds to rank r + 1 (mod C): one
- * cudaMemcpyAsync of its K rows and one of its V rows into the other ring
- * buffer, which is what a point-to-point transfer between two GPUs becomes
- * when all ranks share one.  Events order the two streams: step s + 1 waits
- * for the transfer that filled its slots, and that transfer waits for step
- * s - 1, the last reader of the buffer it overwrites.
+ * every rank sends the shard it holds to rank r + 1 (mod C): its K rows and
+ * its V rows are copied into the other ring buffer, which is what a
+ * point-to-point transfer between two GPUs becomes when all ranks share one.
+ * The copies of a step run as one copy kernel per tensor with a single
+ * small CTA per SM, sized to fit beside the attention kernel's CTAs, so
+ * that they proceed while it computes (a device-to-device cudaMemcpyAsync is
+ * itself a kernel, and launched as the attention kernel starts it takes
+ * every SM first).  Give comm_stream a higher priority than stream.  Events
+ * order the two streams: step s + 1 waits for the transfer that filled its
+ * slots, and that transfer waits for step s - 1, the last reader of the
+ * buffer it overwrites.
  *   q, k, v    : device, sharded order (as cp_attn_fwd)
  *   o, lse     : device, as cp_attn_fwd; lse is also the running accumulator
  *   workspace  : cp_workspace_size(desc, CP_OP_RING_FWD) bytes: the C step
- *                plans, 2 x 2 ring buffers of C x max_rank_rows rows of K and
- *                of V, and (bf16 problems) the fp32 o accumulator
+ *                plans, the copy lists of the transfers, 2 x 2 ring buffers
+ *                of C x max_rank_rows rows of K and of V, and (bf16 problems)
+ *                the fp32 o accumulator
  *                [T, hq, d_v]; fp32 problems accumulate in o itself
  *   stream     : compute stream; the call's results are complete when the
  *                work enqueued on it is (the transfers are ordered before the
