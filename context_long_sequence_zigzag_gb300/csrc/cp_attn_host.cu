@@ -13,6 +13,8 @@
 #include <atomic>
 #include <cmath>
 #include <cstring>
+#include <list>
+#include <memory>
 #include <mutex>
 #include <vector>
 
@@ -279,6 +281,45 @@ size_t plan_bytes(const Plan& p) {
   return align256(p.tiles.size() * sizeof(TileDesc)) + align256(p.ranges.size() * sizeof(RangeDesc));
 }
 
+// Recently built plans.  A plan depends only on the shard map (T, the
+// sequence lengths, C, the layout), the mask and which plan it is, so
+// repeated calls on the same problem (every training step) reuse it instead
+// of rebuilding it on the host; the upload into the call's workspace still
+// happens every call, since the caller may use that memory for anything in
+// between.
+enum PlanKind : int64_t { kPlanQueryMajor = 0, kPlanKeyMajor = 1 };
+std::shared_ptr<const Plan> get_plan(const cp_desc_t* d, const ShardMap& m, PlanKind kind, int q_rank = -1,
+                                     int kv_rank = -1, int ring_step = -1, int64_t slot_rows = 0) {
+  static std::mutex mu;
+  static std::list<std::pair<std::vector<int64_t>, std::shared_ptr<const Plan>>> cache;  // most recent first
+  static size_t cached_bytes = 0;
+  // a ring of C steps uses C plans; bounded by count and by host bytes
+  constexpr size_t kMaxPlans = 80, kMaxBytes = size_t(256) << 20;
+  std::vector<int64_t> key = {kind, q_rank, kv_rank, ring_step, slot_rows, d->total_tokens, d->cp_size, d->layout,
+                              d->causal, d->num_seqs};
+  if (d->cu_seqlens) key.insert(key.end(), d->cu_seqlens, d->cu_seqlens + d->num_seqs + 1);
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    for (auto it = cache.begin(); it != cache.end(); ++it)
+      if (it->first == key) {
+        cache.splice(cache.begin(), cache, it);
+        return it->second;
+      }
+  }
+  auto plan = std::make_shared<Plan>(kind == kPlanKeyMajor ? build_bwd_plan(d, m)
+                                                           : build_fwd_plan(d, m, q_rank, kv_rank, ring_step, slot_rows));
+  order_by_work(*plan);
+  std::lock_guard<std::mutex> lock(mu);
+  cache.emplace_front(std::move(key), plan);
+  cached_bytes += plan_bytes(*plan);
+  while (cache.size() > 1 && (cache.size() > kMaxPlans || cached_bytes > kMaxBytes)) {
+    cached_bytes -= plan_bytes(*cache.back().second);
+    cache.pop_back();
+  }
+  return plan;
+}
+
+
 // Copies the plan into the workspace at `base`; returns the device pointers.
 cudaError_t upload_plan(const Plan& p, char* base, cudaStream_t st, const TileDesc** tiles,
                         const RangeDesc** ranges) {
@@ -350,8 +391,8 @@ AttnArgs base_args(const cp_desc_t* d) {
 // Uploads the key-major plan into `ws` and launches the dK/dV kernel.
 cp_status_t run_bwd_dkdv(const cp_desc_t* d, const ShardMap& m, AttnArgs a, char* ws, size_t ws_bytes,
                          cudaStream_t cs) {
-  Plan pb = build_bwd_plan(d, m);
-  order_by_work(pb);
+  const auto pbp = get_plan(d, m, kPlanKeyMajor);
+  const Plan& pb = *pbp;
   if (ws == nullptr || (reinterpret_cast<uintptr_t>(ws) & 255) || ws_bytes < plan_bytes(pb)) return CP_ERR_WORKSPACE;
   const cp_status_t st = stage_plan(pb, ws, cs, a, d->total_tokens, d->total_tokens);
   if (st != CP_OK) return st;
@@ -362,8 +403,8 @@ cp_status_t run_bwd_dkdv(const cp_desc_t* d, const ShardMap& m, AttnArgs a, char
 // Uploads the query-major plan into `ws` and launches the dQ kernel.
 cp_status_t run_bwd_dq(const cp_desc_t* d, const ShardMap& m, AttnArgs a, char* ws, size_t ws_bytes,
                        cudaStream_t cs) {
-  Plan pf = build_fwd_plan(d, m, -1, -1);
-  order_by_work(pf);
+  const auto pfp = get_plan(d, m, kPlanQueryMajor);
+  const Plan& pf = *pfp;
   if (ws == nullptr || (reinterpret_cast<uintptr_t>(ws) & 255) || ws_bytes < plan_bytes(pf)) return CP_ERR_WORKSPACE;
   const cp_status_t st = stage_plan(pf, ws, cs, a, d->total_tokens, d->total_tokens);
   if (st != CP_OK) return st;
@@ -535,7 +576,7 @@ BwdLayout bwd_layout(const cp_desc_t* d, const Plan& pf, const Plan& pb) {
 // relative to the list's source (k / v at s = 0, else the step's ring
 // buffer) and destination (the other ring buffer).
 struct RingLayout {
-  std::vector<Plan> plans;
+  std::vector<std::shared_ptr<const Plan>> plans;
   std::vector<size_t> plan_off;
   std::vector<CopySeg> segs;       // all lists, back to back
   std::vector<int32_t> seg_begin;  // list l = 2 * s + tensor: segs[seg_begin[l] .. seg_begin[l + 1])
@@ -548,10 +589,9 @@ RingLayout ring_layout(const cp_desc_t* d, const ShardMap& m) {
   for (int r = 0; r < m.C; ++r) L.slot_rows = std::max<int64_t>(L.slot_rows, m.rank_off[r + 1] - m.rank_off[r]);
   size_t off = 0;
   for (int s = 0; s < m.C; ++s) {
-    L.plans.push_back(build_fwd_plan(d, m, -1, -1, s, L.slot_rows));
-    order_by_work(L.plans.back());
+    L.plans.push_back(get_plan(d, m, kPlanQueryMajor, -1, -1, s, L.slot_rows));
     L.plan_off.push_back(off);
-    off += plan_bytes(L.plans.back());
+    off += plan_bytes(*L.plans.back());
   }
   const size_t elt = d->dtype == CP_DT_BF16 ? 2 : 4;
   const int64_t row_bytes[2] = {int64_t(d->hkv) * d->d_qk * int64_t(elt), int64_t(d->hkv) * d->d_v * int64_t(elt)};
@@ -670,7 +710,7 @@ cp_status_t cp_workspace_size(const cp_desc_t* d, int32_t op, size_t* bytes) {
   if (st != CP_OK) return st;
   ShardMap m = build_map(d);
   if (op == CP_OP_FWD) {
-    *bytes = plan_bytes(build_fwd_plan(d, m, -1, -1));
+    *bytes = plan_bytes(*get_plan(d, m, kPlanQueryMajor));
   } else if (op == CP_OP_BLOCK_FWD) {
     // the largest (q rank, kv rank) plan is bounded by the plan of rank q's
     // tiles against all ranks; size for the worst rank
@@ -678,11 +718,11 @@ cp_status_t cp_workspace_size(const cp_desc_t* d, int32_t op, size_t* bytes) {
     for (int r = 0; r < m.C; ++r) mx = std::max(mx, plan_bytes(build_fwd_plan(d, m, r, -1)));
     *bytes = mx;
   } else if (op == CP_OP_BWD) {
-    *bytes = bwd_layout(d, build_fwd_plan(d, m, -1, -1), build_bwd_plan(d, m)).total;
+    *bytes = bwd_layout(d, *get_plan(d, m, kPlanQueryMajor), *get_plan(d, m, kPlanKeyMajor)).total;
   } else if (op == CP_OP_BWD_DKDV) {
-    *bytes = plan_bytes(build_bwd_plan(d, m));
+    *bytes = plan_bytes(*get_plan(d, m, kPlanKeyMajor));
   } else if (op == CP_OP_BWD_DQ) {
-    *bytes = plan_bytes(build_fwd_plan(d, m, -1, -1));
+    *bytes = plan_bytes(*get_plan(d, m, kPlanQueryMajor));
   } else if (op == CP_OP_RING_FWD) {
     *bytes = ring_layout(d, m).total;
   } else if (op == CP_OP_ULYSSES_FWD || op == CP_OP_ULYSSES_BWD) {
@@ -710,7 +750,8 @@ cp_status_t cp_rank_block_counts(const cp_desc_t* d, int64_t* counts) {
   if (st != CP_OK) return st;
   if (counts == nullptr) return CP_ERR_INVALID_ARG;
   ShardMap m = build_map(d);
-  Plan p = build_fwd_plan(d, m, -1, -1);
+  const auto pp = get_plan(d, m, kPlanQueryMajor);
+  const Plan& p = *pp;
   for (int r = 0; r < m.C; ++r) counts[r] = 0;
   for (const TileDesc& t : p.tiles) counts[t.rank] += t.work;
   return CP_OK;
@@ -792,8 +833,8 @@ cp_status_t cp_attn_block_fwd(const cp_desc_t* d, int32_t q_rank, int32_t kv_ran
   if (!q || !k || !v || !o_part || !lse_part) return CP_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o_part) || !aligned16(lse_part))
     return CP_ERR_INVALID_ARG;
-  Plan p = build_fwd_plan(d, m, q_rank, kv_rank);
-  order_by_work(p);
+  const auto pp = get_plan(d, m, kPlanQueryMajor, q_rank, kv_rank);
+  const Plan& p = *pp;
   if (ws == nullptr || (reinterpret_cast<uintptr_t>(ws) & 255) || ws_bytes < plan_bytes(p))
     return CP_ERR_WORKSPACE;
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
@@ -820,8 +861,8 @@ cp_status_t cp_attn_fwd(const cp_desc_t* d, const void* q, const void* k, const 
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
     return CP_ERR_INVALID_ARG;
   ShardMap m = build_map(d);
-  Plan p = build_fwd_plan(d, m, -1, -1);
-  order_by_work(p);
+  const auto pp = get_plan(d, m, kPlanQueryMajor);
+  const Plan& p = *pp;
   if (ws == nullptr || (reinterpret_cast<uintptr_t>(ws) & 255) || ws_bytes < plan_bytes(p))
     return CP_ERR_WORKSPACE;
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
@@ -847,8 +888,10 @@ cp_status_t cp_attn_bwd(const cp_desc_t* d, const void* q, const void* k, const 
   for (const void* p : ptrs)
     if (p == nullptr || !aligned16(p)) return CP_ERR_INVALID_ARG;
   ShardMap m = build_map(d);
-  Plan pf = build_fwd_plan(d, m, -1, -1);
-  Plan pb = build_bwd_plan(d, m);
+  const auto pfp = get_plan(d, m, kPlanQueryMajor);
+  const auto pbp = get_plan(d, m, kPlanKeyMajor);
+  const Plan& pf = *pfp;
+  const Plan& pb = *pbp;
   BwdLayout L = bwd_layout(d, pf, pb);
   if (ws == nullptr || (reinterpret_cast<uintptr_t>(ws) & 255) || ws_bytes < L.total)
     return CP_ERR_WORKSPACE;
@@ -917,8 +960,8 @@ cp_status_t cp_attn_fwd_noalloc(const cp_desc_t* d, const void* q, const void* k
   if (st != CP_OK) return st;
   if (d->total_tokens == 0) return CP_OK;
   ShardMap m = build_map(d);
-  Plan p = build_fwd_plan(d, m, -1, -1);
-  order_by_work(p);
+  const auto pp = get_plan(d, m, kPlanQueryMajor);
+  const Plan& p = *pp;
   if (plan_bytes(p) > CP_NOALLOC_SCRATCH_BYTES) return CP_ERR_WORKSPACE;
   if (!q || !k || !v || !o || !lse) return CP_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
@@ -967,7 +1010,7 @@ cp_status_t cp_ring_attn_fwd(const cp_desc_t* d, const void* q, const void* k, c
     a.lse = lse;
     a.lse_stride = d->total_tokens;
     a.block_mode = s == 0 ? 1 : 2;
-    st = stage_plan(L.plans[s], base + L.plan_off[s], cs, a, d->total_tokens, a.T_kv ? a.T_kv : d->total_tokens);
+    st = stage_plan(*L.plans[s], base + L.plan_off[s], cs, a, d->total_tokens, a.T_kv ? a.T_kv : d->total_tokens);
     if (st != CP_OK) return st;
   }
   cudaEvent_t ev_comp = nullptr, ev_comm = nullptr;
