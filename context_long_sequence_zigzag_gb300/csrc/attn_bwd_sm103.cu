@@ -81,6 +81,21 @@ struct BwdParams {
   int32_t* err;
 };
 
+// Grid order of the query-major kernels: key/value heads outermost, then
+// the tiles (heaviest first), then the query heads of the group, so that the
+// CTAs resident at one time read the K and V of one key/value head, which
+// then stay in L2 (the heads of one tile inside each other instead made the
+// resident CTAs stream every head at once: S=256K with 64 heads of 192,
+// forward 1.61 s against 0.86 s in this order).
+__device__ __forceinline__ void grid_tile_slot(const AttnArgs& a, int& tile_idx, int& slot) {
+  const int G = a.hq / a.hkv;
+  const unsigned per_kv = unsigned(a.num_tiles) * unsigned(G);
+  const int kv = int(blockIdx.x / per_kv);
+  const unsigned rem = blockIdx.x - unsigned(kv) * per_kv;
+  tile_idx = int(rem / unsigned(G));
+  slot = kv * G + int(rem - unsigned(tile_idx) * unsigned(G));
+}
+
 __device__ __forceinline__ int head_of_slot(int slot, const AttnArgs& a) {
   const int G = a.hq / a.hkv;
   const int kv = slot / G, g = slot - kv * G;
@@ -277,8 +292,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dkdv_kernel(const __grid
     if (threadIdx.x == 0 && p.err) atomicCAS(p.err, 0, 0x100 | kSiteAlign);
     return;
   }
-  const int tile_idx = blockIdx.x / a.hkv;
-  const int kvh = blockIdx.x - tile_idx * a.hkv;
+  // key/value heads outermost, then the tiles (heaviest first): the CTAs
+  // resident at one time read one head's Q and dO
+  const int kvh = int(blockIdx.x / unsigned(a.num_tiles));
+  const int tile_idx = int(blockIdx.x - unsigned(kvh) * unsigned(a.num_tiles));
   if (a.debug && !debug_plan_ok(a, tile_idx, kvh, kvh, true, p.err)) return;
   const TileDesc tile = a.tiles[tile_idx];
   const int G = a.hq / a.hkv;
@@ -628,8 +645,9 @@ __global__ void __launch_bounds__(kThreadsDq, 1) attn_bwd_dq_kernel(const __grid
     if (threadIdx.x == 0 && p.err) atomicCAS(p.err, 0, 0x100 | kSiteAlign);
     return;
   }
-  const int tile_idx = blockIdx.x / a.hq;
-  const int h = head_of_slot(blockIdx.x - tile_idx * a.hq, a);
+  int tile_idx, slot;
+  grid_tile_slot(a, tile_idx, slot);
+  const int h = head_of_slot(slot, a);
   const int kvh = a.gqa_interleaved ? h % a.hkv : h / (a.hq / a.hkv);
   if (a.debug && !debug_plan_ok(a, tile_idx, h, kvh, false, p.err)) return;
   const TileDesc tile = a.tiles[tile_idx];
