@@ -155,6 +155,19 @@ ShardMap build_map(const cp_desc_t* d) {
   return m;
 }
 
+// Position given to a merged run (two whole, unmasked zigzag chunks of one
+// rank): keys far in the past (-kMergedPos) or queries far in the future
+// (+kMergedPos), so that the kernels' causal tests see every pair visible.
+constexpr int32_t kMergedPos = 1 << 29;
+
+// Runs are merged only where positions stay far from kMergedPos.
+bool merge_ok(const ShardMap& m, int seq) {
+  if (m.per != 2) return false;
+  int64_t len = 0;
+  for (int r = 0; r < m.C; ++r) len += m.at(r, seq, 0).len + m.at(r, seq, 1).len;
+  return len < kMergedPos / 4;
+}
+
 struct Plan {
   std::vector<TileDesc> tiles;
   std::vector<RangeDesc> ranges;
@@ -190,6 +203,8 @@ Plan build_fwd_plan(const cp_desc_t* d, const ShardMap& m, int q_rank, int kv_ra
         const int rho = ((A.rank - step) % m.C + m.C) % m.C;
         if (kv_rank >= 0 && rho != kv_rank) continue;
         if (ring_step >= 0 && step != ring_step) continue;
+        const size_t first = p.ranges.size();
+        bool whole[2] = {false, false};  // run k covers its whole chunk without a mask
         for (int k = 0; k < m.per; ++k) {
           const Chunk& B = m.at(rho, A.seq, k);
           if (B.len == 0) continue;
@@ -205,9 +220,20 @@ Plan build_fwd_plan(const cp_desc_t* d, const ShardMap& m, int q_rank, int kv_ra
             r.nrows = B.len;
             r.flags = 0;
           }
-          work += ceil_tiles(r.nrows);
+          whole[p.ranges.size() - first] = r.flags == 0 && r.nrows == B.len;
           p.ranges.push_back(r);
         }
+        // A rank's two zigzag chunks of a sequence are adjacent rows: when the
+        // tile sees both whole and unmasked they are one run (short chunks
+        // then share key tiles).  Its keys are all visible, so it carries a
+        // position far in the past instead of either chunk's.
+        if (p.ranges.size() - first == 2 && whole[0] && whole[1] && merge_ok(m, A.seq) &&
+            p.ranges[first + 1].row0 == p.ranges[first].row0 + p.ranges[first].nrows) {
+          p.ranges[first].nrows += p.ranges[first + 1].nrows;
+          p.ranges[first].pos0 = -kMergedPos;
+          p.ranges.pop_back();
+        }
+        for (size_t i = first; i < p.ranges.size(); ++i) work += ceil_tiles(p.ranges[i].nrows);
       }
       t.range_count = int32_t(p.ranges.size()) - t.range_begin;
       t.work = work;
@@ -237,6 +263,8 @@ Plan build_bwd_plan(const cp_desc_t* d, const ShardMap& m) {
       int32_t work = 0;
       for (int step = 0; step < m.C; ++step) {
         const int rho = (B.rank + step) % m.C;
+        const size_t first = p.ranges.size();
+        bool whole[2] = {false, false};  // run k covers its whole chunk without a mask
         for (int k = 0; k < m.per; ++k) {
           const Chunk& A = m.at(rho, B.seq, k);
           if (A.len == 0) continue;
@@ -255,9 +283,18 @@ Plan build_bwd_plan(const cp_desc_t* d, const ShardMap& m) {
             r.pos0 = apos;
             r.flags = 0;
           }
-          work += ceil_tiles(r.nrows);
+          whole[p.ranges.size() - first] = r.flags == 0 && r.nrows == A.len;
           p.ranges.push_back(r);
         }
+        // the two adjacent zigzag chunks of a rank as one query run when both
+        // see the whole key tile (a position far in the future)
+        if (p.ranges.size() - first == 2 && whole[0] && whole[1] && merge_ok(m, B.seq) &&
+            p.ranges[first + 1].row0 == p.ranges[first].row0 + p.ranges[first].nrows) {
+          p.ranges[first].nrows += p.ranges[first + 1].nrows;
+          p.ranges[first].pos0 = kMergedPos;
+          p.ranges.pop_back();
+        }
+        for (size_t i = first; i < p.ranges.size(); ++i) work += ceil_tiles(p.ranges[i].nrows);
       }
       t.range_count = int32_t(p.ranges.size()) - t.range_begin;
       t.work = work;

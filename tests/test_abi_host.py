@@ -82,9 +82,10 @@ def test_shard_offsets_match_oracle(layout, lengths, C):
 
 def _tile_pairs_oracle(cu, C, layout):
     """Visible 128x128 (query tile, key tile) pairs per rank, counted from the
-    oracle's shard order: tiles are cut per chunk from its first row."""
-    perm = oracle.shard_order(cu, C, layout)
-    off = oracle.rank_offsets(cu, C, layout)
+    oracle's chunk bounds: key tiles are cut per chunk from its first row,
+    except that a rank's two zigzag chunks of a sequence, adjacent in its
+    shard, are cut as one run when the query tile sees both of them whole
+    (every key before the tile's first query)."""
     n = C if layout == "contiguous" else 2 * C
     counts = []
     for r in range(C):
@@ -92,18 +93,20 @@ def _tile_pairs_oracle(cu, C, layout):
         for s in range(len(cu) - 1):
             L = cu[s + 1] - cu[s]
             b = oracle.chunk_bounds(L, n)
-            mine = oracle.rank_chunks(r, C, layout)
-            for ca in mine:
+            for ca in oracle.rank_chunks(r, C, layout):
                 for t0 in range(b[ca], b[ca + 1], 128):
                     qmax = min(t0 + 128, b[ca + 1]) - 1
-                    for cb in range(n):
-                        lo, hi = b[cb], b[cb + 1]
-                        if hi <= lo or lo > qmax:
-                            continue
-                        vis = min(hi - lo, qmax - lo + 1)
-                        tot += -(-vis // 128)
+                    for rho in range(C):
+                        runs = []  # (visible rows, whole and unmasked)
+                        for cb in oracle.rank_chunks(rho, C, layout):
+                            lo, hi = b[cb], b[cb + 1]
+                            if hi <= lo or lo > qmax:
+                                continue
+                            runs.append((min(hi - lo, qmax - lo + 1), hi - 1 <= t0))
+                        if layout == "zigzag" and len(runs) == 2 and runs[0][1] and runs[1][1]:
+                            runs = [(runs[0][0] + runs[1][0], True)]
+                        tot += sum(-(-v // 128) for v, _ in runs)
         counts.append(tot)
-    del perm, off
     return counts
 
 
