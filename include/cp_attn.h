@@ -327,8 +327,7 @@ cp_status_t cp_lin_attn_fwd(const cp_desc_t* desc, const void* q, const void* k,
  * = 4 MiB, held by every GPU that loads the library until the process
  * exits).  It calls no cudaMalloc, cudaFree or allocating routine.
  *   - The first call on a device looks up the array's device address (once
- *     per device, on the current device); make that first call before any
- *     stream capture.
+ *     per device, on the current device).
  *   - A problem whose plan needs more than CP_NOALLOC_SCRATCH_BYTES is
  *     rejected with CP_ERR_WORKSPACE before any GPU work is enqueued.
  *   - Every call shares the one array and overwrites it with its own plan:
