@@ -14,6 +14,7 @@
 #include <cmath>
 #include <cstring>
 #include <list>
+#include <map>
 #include <memory>
 #include <mutex>
 #include <vector>
@@ -357,20 +358,123 @@ std::shared_ptr<const Plan> get_plan(const cp_desc_t* d, const ShardMap& m, Plan
 }
 
 
+// Host -> device copies of plans and tables go through a pinned staging
+// ring, one per device.  From pageable memory the runtime may wait for the
+// stream to drain before it stages a large copy (measured: a 128K-token varlen
+// forward's ~0.7 MB plan held the calling thread for a whole earlier forward,
+// 5.4 ms); from pinned memory the copy is queued and the call returns.  A
+// region of the ring is reused only after the event recorded behind its last
+// copy has completed.
+class StagingRing {
+ public:
+  static constexpr size_t kBytes = size_t(32) << 20;
+  static constexpr size_t kTracked = 64;
+
+  // Queues dst <- src (bytes) on st through the ring of the current device;
+  // false when the ring is not usable for this copy (the caller then copies
+  // from the source directly).
+  bool copy(void* dst, const void* src, size_t bytes, cudaStream_t st, cudaError_t* err) {
+    if (bytes == 0 || bytes > kBytes / 4) return false;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return false;
+    std::lock_guard<std::mutex> lock(mu_);
+    PerDevice& r = rings_[dev];
+    if (r.failed) return false;
+    if (!r.host) {
+      if (cudaMallocHost(&r.host, kBytes) != cudaSuccess) {
+        cudaGetLastError();
+        r.host = nullptr;
+        r.failed = true;
+        return false;
+      }
+    }
+    // at most kTracked copies tracked: the oldest has long finished by then
+    while (r.inflight.size() >= kTracked) {
+      cudaEventSynchronize(r.inflight.front().ev);
+      r.free_events.push_back(r.inflight.front().ev);
+      r.inflight.pop_front();
+    }
+    size_t off = align256(r.head);
+    if (off + bytes > kBytes) off = 0;
+    // wait for (normally long finished) copies still reading [off, off + bytes)
+    for (auto it = r.inflight.begin(); it != r.inflight.end();) {
+      if (it->begin < off + bytes && off < it->end) {
+        cudaEventSynchronize(it->ev);
+        r.free_events.push_back(it->ev);
+        it = r.inflight.erase(it);
+      } else {
+        ++it;
+      }
+    }
+    std::memcpy(static_cast<char*>(r.host) + off, src, bytes);
+    *err = cudaMemcpyAsync(dst, static_cast<char*>(r.host) + off, bytes, cudaMemcpyHostToDevice, st);
+    r.head = off + bytes;
+    cudaEvent_t ev = nullptr;
+    if (!r.free_events.empty()) {
+      ev = r.free_events.back();
+      r.free_events.pop_back();
+    } else if (cudaEventCreateWithFlags(&ev, cudaEventDisableTiming) != cudaSuccess) {
+      cudaGetLastError();
+      ev = nullptr;
+    }
+    if (*err == cudaSuccess && ev && cudaEventRecord(ev, st) == cudaSuccess) {
+      r.inflight.push_back({off, off + bytes, ev});
+    } else {
+      // no completion to track (a stream of another device, or no event):
+      // wait for the copy here before the region can be reused
+      cudaGetLastError();
+      if (*err == cudaSuccess) *err = cudaStreamSynchronize(st);
+      if (ev) r.free_events.push_back(ev);
+    }
+    return true;
+  }
+
+ private:
+  struct Span {
+    size_t begin, end;
+    cudaEvent_t ev;
+  };
+  struct PerDevice {
+    void* host = nullptr;
+    bool failed = false;
+    size_t head = 0;
+    std::list<Span> inflight;
+    std::vector<cudaEvent_t> free_events;
+  };
+  std::mutex mu_;
+  std::map<int, PerDevice> rings_;
+};
+
+// Held until the process exits (no destructor runs at exit, when the CUDA
+// runtime may already be gone).
+StagingRing& staging_ring() {
+  static StagingRing* ring = new StagingRing();
+  return *ring;
+}
+
+// dst <- src on st: through the staging ring when `pinned` allows it (every
+// entry point but the allocation-free one), else straight from `src`, which
+// must then stay valid until the runtime has staged it (it has when this
+// returns).
+cudaError_t h2d_async(void* dst, const void* src, size_t bytes, cudaStream_t st, bool pinned = true) {
+  if (bytes == 0) return cudaSuccess;
+  cudaError_t e = cudaSuccess;
+  if (pinned && staging_ring().copy(dst, src, bytes, st, &e)) return e;
+  return cudaMemcpyAsync(dst, src, bytes, cudaMemcpyHostToDevice, st);
+}
+
 // Copies the plan into the workspace at `base`; returns the device pointers.
 cudaError_t upload_plan(const Plan& p, char* base, cudaStream_t st, const TileDesc** tiles,
-                        const RangeDesc** ranges) {
+                        const RangeDesc** ranges, bool pinned = true) {
   const size_t tb = p.tiles.size() * sizeof(TileDesc);
   const size_t rb = p.ranges.size() * sizeof(RangeDesc);
   char* rbase = base + align256(tb);
-  // Pageable source: the runtime stages the bytes before returning, so the
-  // vectors may be freed as soon as these calls return.
   if (tb) {
-    cudaError_t e = cudaMemcpyAsync(base, p.tiles.data(), tb, cudaMemcpyHostToDevice, st);
+    cudaError_t e = h2d_async(base, p.tiles.data(), tb, st, pinned);
     if (e != cudaSuccess) return e;
   }
   if (rb) {
-    cudaError_t e = cudaMemcpyAsync(rbase, p.ranges.data(), rb, cudaMemcpyHostToDevice, st);
+    cudaError_t e = h2d_async(rbase, p.ranges.data(), rb, st, pinned);
     if (e != cudaSuccess) return e;
   }
   *tiles = reinterpret_cast<const TileDesc*>(base);
@@ -387,14 +491,14 @@ std::atomic<int32_t> g_debug_checks{0};
 // range_rows for the runs); an inconsistent plan is refused before any GPU
 // work of the call.
 cp_status_t stage_plan(const Plan& p, char* base, cudaStream_t st, AttnArgs& a, int64_t tile_rows,
-                       int64_t range_rows) {
+                       int64_t range_rows, bool pinned = true) {
   if (a.debug) {
     for (int32_t i = 0; i < int32_t(p.tiles.size()); ++i)
       if (plan_entry_check(p.tiles.data(), int32_t(p.tiles.size()), p.ranges.data(), int32_t(p.ranges.size()), i, 0,
                            1, 0, 1, tile_rows, range_rows, a.block_mode, a.lse_stride) != 0)
         return CP_ERR_INVALID_ARG;
   }
-  if (upload_plan(p, base, st, &a.tiles, &a.ranges) != cudaSuccess) return CP_ERR_CUDA;
+  if (upload_plan(p, base, st, &a.tiles, &a.ranges, pinned) != cudaSuccess) return CP_ERR_CUDA;
   a.num_tiles = int32_t(p.tiles.size());
   a.num_ranges = int32_t(p.ranges.size());
   a.max_ranges = p.max_ranges;
@@ -833,9 +937,7 @@ cp_status_t cp_shard_permute(const cp_desc_t* d, const void* in, void* out, int6
     }
   }
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
-  if (cudaMemcpyAsync(ws, segs.data(), segs.size() * sizeof(CopySeg), cudaMemcpyHostToDevice, cs) !=
-      cudaSuccess)
-    return CP_ERR_CUDA;
+  if (h2d_async(ws, segs.data(), segs.size() * sizeof(CopySeg), cs) != cudaSuccess) return CP_ERR_CUDA;
   if (launch_permute(static_cast<const CopySeg*>(ws), int32_t(segs.size()), pieces, in, out, cs) !=
       cudaSuccess)
     return CP_ERR_CUDA;
@@ -1007,7 +1109,9 @@ cp_status_t cp_attn_fwd_noalloc(const cp_desc_t* d, const void* q, const void* k
   if (noalloc_scratch(&scratch) != cudaSuccess) return CP_ERR_CUDA;
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
   AttnArgs a = base_args(d);
-  st = stage_plan(p, static_cast<char*>(scratch), cs, a, d->total_tokens, d->total_tokens);
+  // straight from the cached plan: this entry point allocates nothing, not
+  // even the staging ring
+  st = stage_plan(p, static_cast<char*>(scratch), cs, a, d->total_tokens, d->total_tokens, false);
   if (st != CP_OK) return st;
   a.q = q;
   a.k = k;
@@ -1063,8 +1167,8 @@ cp_status_t cp_ring_attn_fwd(const cp_desc_t* d, const void* q, const void* k, c
   // after it.  Their columns are masked (P = 0), but 0 times a stale NaN
   // pattern is NaN, so the ring buffers start out zeroed.
   if (cudaMemsetAsync(base + L.kslot[0], 0, L.oacc - L.kslot[0], cs) != cudaSuccess) return cleanup(CP_ERR_CUDA);
-  if (!L.segs.empty() && cudaMemcpyAsync(base + L.segs_off, L.segs.data(), L.segs.size() * sizeof(CopySeg),
-                                         cudaMemcpyHostToDevice, cs) != cudaSuccess)
+  if (!L.segs.empty() && h2d_async(base + L.segs_off, L.segs.data(), L.segs.size() * sizeof(CopySeg), cs) !=
+                             cudaSuccess)
     return cleanup(CP_ERR_CUDA);
   // the inputs (and the uploaded plans) are ready on the compute stream
   if (cudaEventRecord(ev_comp, cs) != cudaSuccess) return cleanup(CP_ERR_CUDA);
@@ -1118,7 +1222,7 @@ cp_status_t cp_ulysses_a2a(const cp_desc_t* d, const void* in, void* out, int32_
   if (ws == nullptr || (reinterpret_cast<uintptr_t>(ws) & 255) || ws_bytes < need) return CP_ERR_WORKSPACE;
   const std::vector<int32_t> perm = sharded_to_global(build_map(d), d->total_tokens);
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
-  if (cudaMemcpyAsync(ws, perm.data(), perm.size() * 4, cudaMemcpyHostToDevice, cs) != cudaSuccess) return CP_ERR_CUDA;
+  if (h2d_async(ws, perm.data(), perm.size() * 4, cs) != cudaSuccess) return CP_ERR_CUDA;
   const int64_t chunk = int64_t(heads / d->cp_size) * head_bytes;
   return launch_ulysses_a2a(static_cast<const int32_t*>(ws), d->total_tokens, d->cp_size, chunk, in, out, inverse,
                             cs) == cudaSuccess
@@ -1143,7 +1247,7 @@ cp_status_t cp_ulysses_attn_fwd(const cp_desc_t* d, const void* q, const void* k
   char* base = static_cast<char*>(ws);
   const int32_t* perm = reinterpret_cast<const int32_t*>(base + L.perm);
   const std::vector<int32_t> hperm = sharded_to_global(build_map(d), d->total_tokens);
-  if (cudaMemcpyAsync(base + L.perm, hperm.data(), hperm.size() * 4, cudaMemcpyHostToDevice, cs) != cudaSuccess)
+  if (h2d_async(base + L.perm, hperm.data(), hperm.size() * 4, cs) != cudaSuccess)
     return CP_ERR_CUDA;
   const int64_t T = d->total_tokens;
   const int C = d->cp_size, elt = d->dtype == CP_DT_BF16 ? 2 : 4;
@@ -1181,7 +1285,7 @@ cp_status_t cp_ulysses_attn_bwd(const cp_desc_t* d, const void* q, const void* k
   char* base = static_cast<char*>(ws);
   const int32_t* perm = reinterpret_cast<const int32_t*>(base + L.perm);
   const std::vector<int32_t> hperm = sharded_to_global(build_map(d), d->total_tokens);
-  if (cudaMemcpyAsync(base + L.perm, hperm.data(), hperm.size() * 4, cudaMemcpyHostToDevice, cs) != cudaSuccess)
+  if (h2d_async(base + L.perm, hperm.data(), hperm.size() * 4, cs) != cudaSuccess)
     return CP_ERR_CUDA;
   const int64_t T = d->total_tokens;
   const int C = d->cp_size, elt = d->dtype == CP_DT_BF16 ? 2 : 4;
@@ -1219,10 +1323,8 @@ cp_status_t cp_lin_attn_fwd(const cp_desc_t* d, const void* q, const void* k, co
   if (B.blocks.empty()) return CP_OK;
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
   char* base = static_cast<char*>(ws);
-  if (cudaMemcpyAsync(base + L.blocks, B.blocks.data(), B.blocks.size() * sizeof(LinBlock), cudaMemcpyHostToDevice,
-                      cs) != cudaSuccess ||
-      cudaMemcpyAsync(base + L.seq_begin, B.seq_begin.data(), B.seq_begin.size() * 4, cudaMemcpyHostToDevice, cs) !=
-          cudaSuccess)
+  if (h2d_async(base + L.blocks, B.blocks.data(), B.blocks.size() * sizeof(LinBlock), cs) != cudaSuccess ||
+      h2d_async(base + L.seq_begin, B.seq_begin.data(), B.seq_begin.size() * 4, cs) != cudaSuccess)
     return CP_ERR_CUDA;
   return launch_lin_attn(reinterpret_cast<const LinBlock*>(base + L.blocks), int32_t(B.blocks.size()),
                          reinterpret_cast<const int32_t*>(base + L.seq_begin), m.S, d->hq, d->total_tokens, d->d_qk,

@@ -23,9 +23,14 @@
  *     "位置编码必须跟序列分片一起走" (all position metadata follows the shard map).
  *
  * Conventions shared by every entry point
- *   - Ownership: the caller owns every buffer; the library never allocates or
- *     frees memory.  Device buffers are plain device pointers; the host
- *     pointers are read during the call only.
+ *   - Ownership: the caller owns every buffer; the library allocates no
+ *     device memory.  Device buffers are plain device pointers; the host
+ *     pointers are read during the call only.  For its host-to-device copies
+ *     of tile plans and index tables the library keeps one pinned host
+ *     staging buffer of 32 MiB per device, allocated by the first call on
+ *     that device that needs it and held until the process exits, so that a
+ *     call does not wait for earlier work on its stream (cp_attn_fwd_noalloc
+ *     never uses it).
  *   - Streams: all GPU work is enqueued asynchronously on `stream` (a
  *     cudaStream_t; NULL = the legacy default stream).  A call returns after
  *     enqueueing; errors found on the host are returned before anything is
