@@ -315,6 +315,9 @@ __global__ void __launch_bounds__(224, 1) attn_fwd_tc_kernel(const __grid_consta
     float m_ref = row_ok ? -INFINITY : 0.f;
     float l = 0.f;
     bool ok = true;
+    // A warp whose 32 rows all lie past a ragged tile only keeps the barrier
+    // phases: P of those TMEM lanes feeds only O rows that are never stored.
+    const bool idle_warp = __all_sync(0xffffffffu, !row_ok);
     KvCursor cur;
     cur.init(a.ranges, tile.range_begin, tile.range_count);
     for (int j = 0; j < n_kv; ++j, cur.next()) {
@@ -323,6 +326,12 @@ __global__ void __launch_bounds__(224, 1) attn_fwd_tc_kernel(const __grid_consta
       if (!__all_sync(0xffffffffu, ptx::mbar_wait_poll(bar_s_full(sb), (j / Cfg::NS_S) & 1, kSiteSFull, wctx))) {
         ok = false;
         break;
+      }
+      if (idle_warp) {
+        // arrive only after S(j): one arrival per phase of the buffer's barrier
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(bar_p_full(sb));
+        continue;
       }
       ptx::tc_fence_after();
       uint32_t sr[4][32];
