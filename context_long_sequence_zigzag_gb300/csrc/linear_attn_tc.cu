@@ -250,7 +250,8 @@ constexpr uint32_t kStage = 3 * kTile;  // Q, K, V
 constexpr uint32_t offHb = 2 * kStage;
 constexpr uint32_t offBarO = offHb + kTile;
 constexpr int kNumBarsO = 2 + 2 + 5;
-constexpr uint32_t kOutSmem = offBarO + kNumBarsO * 8 + 16;
+constexpr uint32_t offTabO = offBarO + kNumBarsO * 8 + 16;  // alpha^d, d = 0..127 (fp32)
+constexpr uint32_t kOutSmem = offTabO + kC * 4;
 static_assert(kOutSmem <= 232448, "shared memory budget");
 
 __global__ void __launch_bounds__(kOutThreads, 1) lin_output_tc_kernel(const __grid_constant__ LinTcParams p) {
@@ -388,6 +389,11 @@ __global__ void __launch_bounds__(kOutThreads, 1) lin_output_tc_kernel(const __g
     const uint32_t lane_base = uint32_t(warp * 32) << 16;
     uint8_t* Hb = smem + offHb;
     bool ok = true;
+    // alpha^d for every distance d inside a chunk, computed once: the decay
+    // mask then takes a table entry per element instead of an exponential
+    float* dec = reinterpret_cast<float*>(smem + offTabO);
+    dec[r] = ptx::ex2(gl2 * float(r));
+    ptx::named_barrier(1, 128);
     // carried-in state -> TMEM (fp32) and the bf16 copy for the first Q H;
     // all 32 loads of the row are issued before any is used
     {
@@ -446,8 +452,8 @@ __global__ void __launch_bounds__(kOutThreads, 1) lin_output_tc_kernel(const __g
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
             const int s0 = k * 32 + 2 * i;
-            const float d0 = s0 < lim ? ptx::ex2(gl2 * float(r - s0)) : 0.f;
-            const float d1 = s0 + 1 < lim ? ptx::ex2(gl2 * float(r - s0 - 1)) : 0.f;
+            const float d0 = s0 < lim ? dec[r - s0] : 0.f;
+            const float d1 = s0 + 1 < lim ? dec[r - s0 - 1] : 0.f;
             pk[i] = ptx::pack_bf16(__uint_as_float(x[2 * i]) * d0, __uint_as_float(x[2 * i + 1]) * d1);
           }
           ptx::tmem_st16(tA + lane_base + k * 16, pk);
