@@ -83,21 +83,24 @@ __device__ __forceinline__ void scale_row_bf16(uint8_t* tile, int r, float w) {
 // bf16 tile in the 128B-swizzled layout (16-byte chunk q of row r sits at
 // chunk q ^ (r % 8) of its 128-byte row).
 __device__ __forceinline__ void tmem_row_to_swizzled_bf16(uint32_t taddr, uint8_t* tile, int r) {
-#pragma unroll 1
+  // all 128 columns in flight at once: one TMEM round trip, not four
+  uint32_t x[4][32];
+#pragma unroll
+  for (int c = 0; c < 4; ++c) ptx::tmem_ld32(taddr + c * 32, x[c]);
+  ptx::tmem_ld_wait();
+#pragma unroll
+  for (int c = 0; c < 4; ++c) ptx::reg_fence32(x[c]);
+#pragma unroll
   for (int c = 0; c < 4; ++c) {  // 32 columns = 4 chunks of 8
-    uint32_t x[32];
-    ptx::tmem_ld32(taddr + c * 32, x);
-    ptx::tmem_ld_wait();
-    ptx::reg_fence32(x);
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
       const int col = c * 32 + k * 8;
       const int p = col >> 6, q = (col & 63) >> 3;
       uint4 u;
-      u.x = ptx::pack_bf16(__uint_as_float(x[8 * k + 0]), __uint_as_float(x[8 * k + 1]));
-      u.y = ptx::pack_bf16(__uint_as_float(x[8 * k + 2]), __uint_as_float(x[8 * k + 3]));
-      u.z = ptx::pack_bf16(__uint_as_float(x[8 * k + 4]), __uint_as_float(x[8 * k + 5]));
-      u.w = ptx::pack_bf16(__uint_as_float(x[8 * k + 6]), __uint_as_float(x[8 * k + 7]));
+      u.x = ptx::pack_bf16(__uint_as_float(x[c][8 * k + 0]), __uint_as_float(x[c][8 * k + 1]));
+      u.y = ptx::pack_bf16(__uint_as_float(x[c][8 * k + 2]), __uint_as_float(x[c][8 * k + 3]));
+      u.z = ptx::pack_bf16(__uint_as_float(x[c][8 * k + 4]), __uint_as_float(x[c][8 * k + 5]));
+      u.w = ptx::pack_bf16(__uint_as_float(x[c][8 * k + 6]), __uint_as_float(x[c][8 * k + 7]));
       *reinterpret_cast<uint4*>(tile + p * kPanel + r * 128 + ((q ^ (r & 7)) << 4)) = u;
     }
   }
@@ -438,44 +441,46 @@ __global__ void __launch_bounds__(kOutThreads, 1) lin_output_tc_kernel(const __g
       if (!ok) break;
       ptx::tc_fence_after();
       // ---- A'[t][s] = A[t][s] alpha^(t-s) for s <= t, s < n (bf16 into TMEM A).
-      // 32 columns at a time: the packed chunk k lands in columns [16k, 16k+16),
-      // which held fp32 columns this thread has already read.
+      // All 128 columns are loaded first (one TMEM round trip); the packed
+      // chunk k then lands in columns [16k, 16k+16).
       {
         const int lim = min(r + 1, n);  // visible columns [0, lim)
-#pragma unroll 1
+        uint32_t x[4][32];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) ptx::tmem_ld32(tA + lane_base + k * 32, x[k]);
+        ptx::tmem_ld_wait();
+#pragma unroll
+        for (int k = 0; k < 4; ++k) ptx::reg_fence32(x[k]);
+#pragma unroll
         for (int k = 0; k < 4; ++k) {
-          uint32_t x[32];
-          ptx::tmem_ld32(tA + lane_base + k * 32, x);
-          ptx::tmem_ld_wait();
-          ptx::reg_fence32(x);
           uint32_t pk[16];
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
             const int s0 = k * 32 + 2 * i;
             const float d0 = s0 < lim ? dec[r - s0] : 0.f;
             const float d1 = s0 + 1 < lim ? dec[r - s0 - 1] : 0.f;
-            pk[i] = ptx::pack_bf16(__uint_as_float(x[2 * i]) * d0, __uint_as_float(x[2 * i + 1]) * d1);
+            pk[i] = ptx::pack_bf16(__uint_as_float(x[k][2 * i]) * d0, __uint_as_float(x[k][2 * i + 1]) * d1);
           }
           ptx::tmem_st16(tA + lane_base + k * 16, pk);
         }
       }
-      // ---- K' = K with row s scaled by alpha^(n-1-s) (0 past the chunk), in place
+      // ---- H *= alpha^n, its TMEM loads in flight while K' = K with row s
+      // scaled by alpha^(n-1-s) (0 past the chunk) is formed in place
       {
+        uint32_t x[4][32];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) ptx::tmem_ld32(tH + lane_base + k * 32, x[k]);
         const float w = r < n ? ptx::ex2(gl2 * float(n - 1 - r)) : 0.f;
         scale_row_bf16(smem + st * kStage + kTile, r, w);
-      }
-      // ---- H *= alpha^n
-      {
         const float an = ptx::ex2(gl2 * float(n));
-#pragma unroll 1
-        for (int k = 0; k < 4; ++k) {
-          uint32_t x[32];
-          ptx::tmem_ld32(tH + lane_base + k * 32, x);
-          ptx::tmem_ld_wait();
-          ptx::reg_fence32(x);
+        ptx::tmem_ld_wait();
 #pragma unroll
-          for (int i = 0; i < 32; ++i) x[i] = __float_as_uint(__uint_as_float(x[i]) * an);
-          ptx::tmem_st32(tH + lane_base + k * 32, x);
+        for (int k = 0; k < 4; ++k) ptx::reg_fence32(x[k]);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) x[k][i] = __float_as_uint(__uint_as_float(x[k][i]) * an);
+          ptx::tmem_st32(tH + lane_base + k * 32, x[k]);
         }
       }
       ptx::tmem_st_wait();
@@ -492,27 +497,36 @@ __global__ void __launch_bounds__(kOutThreads, 1) lin_output_tc_kernel(const __g
         const float dy = ptx::ex2(gl2 * float(r + 1));
         __nv_bfloat16* dst = p.o + ((int64_t(bl.row0) + c * kC + r) * p.H + h) * kD;
 #pragma unroll 1
-        for (int k = 0; k < 4; ++k) {
-          uint32_t x[32], y[32];
-          ptx::tmem_ld32(tX + lane_base + k * 32, x);
-          ptx::tmem_ld32(tY + lane_base + k * 32, y);
+        for (int hh = 0; hh < 2; ++hh) {  // 64 columns of X and Y per TMEM round trip
+          uint32_t x[2][32], y[2][32];
+#pragma unroll
+          for (int k = 0; k < 2; ++k) {
+            ptx::tmem_ld32(tX + lane_base + (2 * hh + k) * 32, x[k]);
+            ptx::tmem_ld32(tY + lane_base + (2 * hh + k) * 32, y[k]);
+          }
           ptx::tmem_ld_wait();
-          ptx::reg_fence32(x);
-          ptx::reg_fence32(y);
+#pragma unroll
+          for (int k = 0; k < 2; ++k) {
+            ptx::reg_fence32(x[k]);
+            ptx::reg_fence32(y[k]);
+          }
           if (r < n) {
-            uint4* d4 = reinterpret_cast<uint4*>(dst + k * 32);
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              float v[8];
+            for (int k = 0; k < 2; ++k) {
+              uint4* d4 = reinterpret_cast<uint4*>(dst + (2 * hh + k) * 32);
 #pragma unroll
-              for (int e = 0; e < 8; ++e)
-                v[e] = p.scale * fmaf(dy, __uint_as_float(y[8 * i + e]), __uint_as_float(x[8 * i + e]));
-              uint4 u;
-              u.x = ptx::pack_bf16(v[0], v[1]);
-              u.y = ptx::pack_bf16(v[2], v[3]);
-              u.z = ptx::pack_bf16(v[4], v[5]);
-              u.w = ptx::pack_bf16(v[6], v[7]);
-              d4[i] = u;
+              for (int i = 0; i < 4; ++i) {
+                float v[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e)
+                  v[e] = p.scale * fmaf(dy, __uint_as_float(y[k][8 * i + e]), __uint_as_float(x[k][8 * i + e]));
+                uint4 u;
+                u.x = ptx::pack_bf16(v[0], v[1]);
+                u.y = ptx::pack_bf16(v[2], v[3]);
+                u.z = ptx::pack_bf16(v[4], v[5]);
+                u.w = ptx::pack_bf16(v[6], v[7]);
+                d4[i] = u;
+              }
             }
           }
         }
