@@ -558,8 +558,9 @@ def ring_measure(r: Runner, steps: int = 3, warmup: int = 2) -> dict:
 
 def aux_bandwidth(r: "Runner", reps: int = 5) -> dict:
     """HBM throughput of the bandwidth-bound kernels on buffers larger than L2:
-    the shard permutation of q (one launch) and one LSE merge of fp32
-    partials over all rows and heads (the stepwise ring's update)."""
+    the shard permutation of q (one launch), one LSE merge of fp32 partials
+    over all rows and heads (the stepwise ring's update) and the backward's
+    pre-pass D = rowsum(dout * o)."""
     cpa, w, dev = r.cpa, r.w, r.dev
     out = {}
     ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
@@ -593,6 +594,19 @@ def aux_bandwidth(r: "Runner", reps: int = 5) -> dict:
     out["lse_merge"] = {"bytes": nbytes, "ms": round(min(times), 4),
                         "gbs": round(nbytes / (min(times) * 1e-3) / 1e9, 1)}
     del o_acc, o_part, l_acc, l_part, y
+    # the backward's pre-pass D = rowsum(dout * o): reads o and dout, writes D
+    dp = torch.empty(w.hq, w.total_tokens, dtype=torch.float32, device=dev)
+    nbytes = 2 * r.o.numel() * r.o.element_size() + dp.numel() * 4
+    times = []
+    for i in range(reps + 1):
+        ev[0].record()
+        cpa.cp_attn_bwd_prep(r.prob, r.o, r.s["dout"], dp)
+        ev[1].record()
+        torch.cuda.synchronize()
+        if i:
+            times.append(ev[0].elapsed_time(ev[1]))
+    out["bwd_preprocess"] = {"bytes": nbytes, "ms": round(min(times), 4),
+                             "gbs": round(nbytes / (min(times) * 1e-3) / 1e9, 1)}
     return out
 
 

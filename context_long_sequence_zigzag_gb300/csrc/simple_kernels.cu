@@ -292,6 +292,42 @@ __global__ void __launch_bounds__(256) bwd_preprocess_kernel(const AttnArgs a) {
   }
 }
 
+// The same for bf16 rows of 8*DV8 values: DV8 lanes per row, one 16-byte
+// load of o and of dout each, so a warp covers 32/DV8 rows at a time.  Rows
+// are taken in (head, token) order, so the D values a warp writes sit next
+// to each other.
+template <int DV8>
+__global__ void __launch_bounds__(256) bwd_preprocess_bf16_kernel(const AttnArgs a) {
+  constexpr int kRows = 32 / DV8;  // rows per warp
+  const int lane = threadIdx.x & 31, sub = lane / DV8, part = lane - sub * DV8;
+  const int64_t nrows = a.T * a.hq;
+  const int64_t step = int64_t(gridDim.x) * (blockDim.x >> 5) * kRows;
+  for (int64_t i0 = (int64_t(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5)) * kRows; i0 < nrows; i0 += step) {
+    const int64_t i = i0 + sub;  // (head, token) pair of this lane group
+    float s = 0.f;
+    int64_t h = 0, t = 0;
+    if (i < nrows) {
+      h = i / a.T;
+      t = i - h * a.T;
+      const int64_t off = (t * a.hq + h) * (8 * DV8) + 8 * part;
+      const uint4 ov = *reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(a.o) + off);
+      const uint4 dv = *reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(a.dout) + off);
+      const uint32_t* o32 = reinterpret_cast<const uint32_t*>(&ov);
+      const uint32_t* d32 = reinterpret_cast<const uint32_t*>(&dv);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float2 of = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&o32[e]));
+        const float2 df = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&d32[e]));
+        s = fmaf(of.x, df.x, s);
+        s = fmaf(of.y, df.y, s);
+      }
+    }
+#pragma unroll
+    for (int m = DV8 / 2; m > 0; m >>= 1) s += __shfl_xor_sync(0xffffffffu, s, m);
+    if (part == 0 && i < nrows) a.dpsum[h * a.T + t] = s;
+  }
+}
+
 // dq for one query row per warp (query-major plan).
 template <typename E>
 __global__ void __launch_bounds__(256) simt_bwd_dq_kernel(const AttnArgs a) {
@@ -499,6 +535,10 @@ cudaError_t launch_simt_fwd(const AttnArgs& args, int32_t dtype, cudaStream_t st
 }
 
 cudaError_t launch_bwd_preprocess(const AttnArgs& a, int32_t dtype, cudaStream_t st) {
+  if (dtype != CP_DT_F32 && a.d_v == 128 && ((reinterpret_cast<uintptr_t>(a.o) | reinterpret_cast<uintptr_t>(a.dout)) & 15) == 0) {
+    bwd_preprocess_bf16_kernel<16><<<unsigned(grid_for(a.T * a.hq, 16)), 256, 0, st>>>(a);
+    return cudaGetLastError();
+  }
   const int64_t grid = grid_for(a.T * a.hq, 8);
   if (dtype == CP_DT_F32)
     bwd_preprocess_kernel<float><<<unsigned(grid), 256, 0, st>>>(a);
