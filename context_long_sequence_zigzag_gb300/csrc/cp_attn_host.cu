@@ -417,12 +417,18 @@ class StagingRing {
       cudaGetLastError();
       ev = nullptr;
     }
-    if (*err == cudaSuccess && ev && cudaEventRecord(ev, st) == cudaSuccess) {
-      r.inflight.push_back({off, off + bytes, ev});
-    } else {
-      // no completion to track (a stream of another device, or no event):
-      // wait for the copy here before the region can be reused
-      cudaGetLastError();
+    bool tracked = false;
+    if (*err == cudaSuccess && ev) {
+      if (cudaEventRecord(ev, st) == cudaSuccess) {
+        r.inflight.push_back({off, off + bytes, ev});
+        tracked = true;
+      } else {
+        cudaGetLastError();  // this failed record's own error (e.g. a stream of another device)
+      }
+    }
+    if (!tracked) {
+      // no completion to track: wait for the copy here before the region can
+      // be reused (a failed copy leaves its error for the caller to read)
       if (*err == cudaSuccess) *err = cudaStreamSynchronize(st);
       if (ev) r.free_events.push_back(ev);
     }
