@@ -84,7 +84,7 @@ def build(verbose: bool = False, extra_flags=None) -> str:
                 if r.returncode != 0:
                     raise RuntimeError("nvcc failed: " + " ".join(cmd))
     if jobs or _stale(LIB, objs):
-        cmd = [nvcc, *ARCH, "-shared", "-o", LIB, *objs, "-Xcompiler", "-fPIC"]
+        cmd = [nvcc, *ARCH, "-shared", "-o", LIB, *objs, "-Xcompiler", "-fPIC", "-ldl"]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if verbose or r.returncode != 0:
             sys.stderr.write(r.stdout + r.stderr)

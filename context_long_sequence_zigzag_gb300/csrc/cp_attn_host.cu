@@ -19,11 +19,24 @@
 #include <mutex>
 #include <vector>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "internal.h"
 #include "plan_check.cuh"
 
 namespace cpattn {
 namespace {
+
+// A named NVTX range around every entry point that enqueues GPU work, so that
+// a profiler's timeline attributes kernels to calls (a no-op without one).
+// The allocation-free forward has none: a profiler's NVTX handler may
+// allocate.
+struct CallRange {
+  explicit CallRange(const char* name) { nvtxRangePushA(name); }
+  ~CallRange() { nvtxRangePop(); }
+  CallRange(const CallRange&) = delete;
+  CallRange& operator=(const CallRange&) = delete;
+};
 
 // One rank's run of one sequence, stored contiguously in sharded order.  Its
 // tokens sit at global rows grow0, grow0 + stride, ... (stride 1 except for
@@ -906,6 +919,7 @@ cp_status_t cp_rank_block_counts(const cp_desc_t* d, int64_t* counts) {
 
 cp_status_t cp_shard_permute(const cp_desc_t* d, const void* in, void* out, int64_t row_bytes,
                              int32_t inverse, void* ws, size_t ws_bytes, cp_stream_t stream) {
+  CallRange range_("cp_shard_permute");
   cp_status_t st = check_map_fields(d);
   if (st != CP_OK) return st;
   if (row_bytes <= 0 || row_bytes % 16 != 0) return CP_ERR_INVALID_ARG;
@@ -952,6 +966,7 @@ cp_status_t cp_shard_permute(const cp_desc_t* d, const void* in, void* out, int6
 
 cp_status_t cp_lse_merge(const cp_desc_t* d, int64_t rows, float* o_acc, float* lse_acc,
                          const float* o_part, const float* lse_part, cp_stream_t stream) {
+  CallRange range_("cp_lse_merge");
   if (d == nullptr || rows < 0) return CP_ERR_INVALID_ARG;
   if (d->hq < 1 || d->d_v < 4 || d->d_v % 4 != 0) return CP_ERR_INVALID_ARG;
   if (rows == 0) return CP_OK;
@@ -968,6 +983,7 @@ cp_status_t cp_lse_merge(const cp_desc_t* d, int64_t rows, float* o_acc, float* 
 cp_status_t cp_attn_block_fwd(const cp_desc_t* d, int32_t q_rank, int32_t kv_rank, const void* q,
                               const void* k, const void* v, float* o_part, float* lse_part, void* ws,
                               size_t ws_bytes, cp_stream_t stream) {
+  CallRange range_("cp_attn_block_fwd");
   cp_status_t st = check_attn_fields(d);
   if (st != CP_OK) return st;
   if (q_rank < 0 || q_rank >= d->cp_size || kv_rank < 0 || kv_rank >= d->cp_size)
@@ -999,6 +1015,7 @@ cp_status_t cp_attn_block_fwd(const cp_desc_t* d, int32_t q_rank, int32_t kv_ran
 
 cp_status_t cp_attn_fwd(const cp_desc_t* d, const void* q, const void* k, const void* v, void* o,
                         float* lse, void* ws, size_t ws_bytes, cp_stream_t stream) {
+  CallRange range_("cp_attn_fwd");
   cp_status_t st = check_attn_fields(d);
   if (st != CP_OK) return st;
   if (d->total_tokens == 0) return CP_OK;
@@ -1026,6 +1043,7 @@ cp_status_t cp_attn_fwd(const cp_desc_t* d, const void* q, const void* k, const 
 cp_status_t cp_attn_bwd(const cp_desc_t* d, const void* q, const void* k, const void* v,
                         const void* o, const float* lse, const void* dout, void* dq, void* dk,
                         void* dv, void* ws, size_t ws_bytes, cp_stream_t stream) {
+  CallRange range_("cp_attn_bwd");
   cp_status_t st = check_attn_fields(d);
   if (st != CP_OK) return st;
   if (d->total_tokens == 0) return CP_OK;
@@ -1057,6 +1075,7 @@ cp_status_t cp_attn_bwd(const cp_desc_t* d, const void* q, const void* k, const 
 }
 
 cp_status_t cp_attn_bwd_prep(const cp_desc_t* d, const void* o, const void* dout, float* dpsum, cp_stream_t stream) {
+  CallRange range_("cp_attn_bwd_prep");
   cp_status_t st = check_attn_fields(d);
   if (st != CP_OK) return st;
   if (d->total_tokens == 0) return CP_OK;
@@ -1073,6 +1092,7 @@ cp_status_t cp_attn_bwd_prep(const cp_desc_t* d, const void* o, const void* dout
 cp_status_t cp_attn_bwd_dkdv(const cp_desc_t* d, const void* q, const void* k, const void* v, const float* lse,
                              const float* dpsum, const void* dout, void* dk, void* dv, void* ws, size_t ws_bytes,
                              cp_stream_t stream) {
+  CallRange range_("cp_attn_bwd_dkdv");
   cp_status_t st = check_attn_fields(d);
   if (st != CP_OK) return st;
   if (d->total_tokens == 0) return CP_OK;
@@ -1088,6 +1108,7 @@ cp_status_t cp_attn_bwd_dkdv(const cp_desc_t* d, const void* q, const void* k, c
 cp_status_t cp_attn_bwd_dq(const cp_desc_t* d, const void* q, const void* k, const void* v, const float* lse,
                            const float* dpsum, const void* dout, void* dq, void* ws, size_t ws_bytes,
                            cp_stream_t stream) {
+  CallRange range_("cp_attn_bwd_dq");
   cp_status_t st = check_attn_fields(d);
   if (st != CP_OK) return st;
   if (d->total_tokens == 0) return CP_OK;
@@ -1130,6 +1151,7 @@ cp_status_t cp_attn_fwd_noalloc(const cp_desc_t* d, const void* q, const void* k
 
 cp_status_t cp_ring_attn_fwd(const cp_desc_t* d, const void* q, const void* k, const void* v, void* o, float* lse,
                              void* ws, size_t ws_bytes, cp_stream_t stream, cp_stream_t comm_stream) {
+  CallRange range_("cp_ring_attn_fwd");
   cp_status_t st = check_attn_fields(d);
   if (st != CP_OK) return st;
   if (d->total_tokens == 0) return CP_OK;
@@ -1214,6 +1236,7 @@ cp_status_t cp_ring_attn_fwd(const cp_desc_t* d, const void* q, const void* k, c
 
 cp_status_t cp_ulysses_a2a(const cp_desc_t* d, const void* in, void* out, int32_t heads, int64_t head_bytes,
                            int32_t inverse, void* ws, size_t ws_bytes, cp_stream_t stream) {
+  CallRange range_("cp_ulysses_a2a");
   cp_status_t st = check_map_fields(d);
   if (st != CP_OK) return st;
   if (heads < 1 || heads % d->cp_size != 0 || head_bytes <= 0 || head_bytes % 16 != 0) return CP_ERR_INVALID_ARG;
@@ -1238,6 +1261,7 @@ cp_status_t cp_ulysses_a2a(const cp_desc_t* d, const void* in, void* out, int32_
 
 cp_status_t cp_ulysses_attn_fwd(const cp_desc_t* d, const void* q, const void* k, const void* v, void* o,
                                 float* lse, void* ws, size_t ws_bytes, cp_stream_t stream) {
+  CallRange range_("cp_ulysses_attn_fwd");
   cp_status_t st = check_attn_fields(d);
   if (st != CP_OK) return st;
   st = check_ulysses(d);
@@ -1276,6 +1300,7 @@ cp_status_t cp_ulysses_attn_fwd(const cp_desc_t* d, const void* q, const void* k
 cp_status_t cp_ulysses_attn_bwd(const cp_desc_t* d, const void* q, const void* k, const void* v, const void* o,
                                 const float* lse, const void* dout, void* dq, void* dk, void* dv, void* ws,
                                 size_t ws_bytes, cp_stream_t stream) {
+  CallRange range_("cp_ulysses_attn_bwd");
   cp_status_t st = check_attn_fields(d);
   if (st != CP_OK) return st;
   st = check_ulysses(d);
@@ -1316,6 +1341,7 @@ cp_status_t cp_ulysses_attn_bwd(const cp_desc_t* d, const void* q, const void* k
 
 cp_status_t cp_lin_attn_fwd(const cp_desc_t* d, const void* q, const void* k, const void* v, const float* g, void* o,
                             void* ws, size_t ws_bytes, cp_stream_t stream) {
+  CallRange range_("cp_lin_attn_fwd");
   cp_status_t st = check_lin(d);
   if (st != CP_OK) return st;
   if (d->total_tokens == 0) return CP_OK;

@@ -31,6 +31,10 @@
  *     that device that needs it and held until the process exits, so that a
  *     call does not wait for earlier work on its stream (cp_attn_fwd_noalloc
  *     never uses it).
+ *   - Tracing: every entry point that enqueues GPU work (but
+ *     cp_attn_fwd_noalloc) opens an NVTX range named after itself for its
+ *     duration on the host, so that a profiler's timeline attributes the
+ *     kernels to the call; without a profiler attached this costs nothing.
  *   - Streams: all GPU work is enqueued asynchronously on `stream` (a
  *     cudaStream_t; NULL = the legacy default stream).  A call returns after
  *     enqueueing; errors found on the host are returned before anything is
