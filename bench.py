@@ -136,6 +136,32 @@ def l2_note(w: workloads.Workload) -> str:
     return f"q is {mib:.1f} MiB, smaller than L2, not flushed between steps"
 
 
+def chosen_workload(args) -> workloads.Workload:
+    """The --workload preset with the command line's overrides applied; an
+    overridden workload's name lists them."""
+    w = workloads.get(args.workload)
+    kw = {}
+    if args.layout:
+        kw["layout"] = args.layout
+    if args.cp_size:
+        kw["cp_size"] = args.cp_size
+    if args.seed is not None:
+        kw["seed"] = args.seed
+    if args.heads:
+        hq, hkv = (int(x) for x in args.heads.split(":"))
+        if hq < 1 or hkv < 1 or hq % hkv:
+            raise SystemExit("--heads wants HQ:HKV with HKV dividing HQ")
+        kw["hq"], kw["hkv"] = hq, hkv
+    if args.seq_len:
+        if w.seqlens is not None or w.varlen_range is not None:
+            raise SystemExit("--seq-len applies to single-sequence workloads")
+        kw["total_tokens"] = args.seq_len
+    if not kw:
+        return w
+    tag = ",".join(f"{k}={v}" for k, v in kw.items())
+    return w.replace(name=f"{w.name}[{tag}]", **kw)
+
+
 def cpu_cores() -> int:
     return _host_cores()
 
@@ -632,9 +658,7 @@ def run_gpu(args):
         dist.init_process_group("nccl")
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
-    w = workloads.get(args.workload)
-    if args.layout:
-        w = w.replace(layout=args.layout)
+    w = chosen_workload(args)
     r = Runner(w, dev)
     cpa = r.cpa
 
@@ -673,7 +697,7 @@ def run_gpu(args):
     aux = aux_bandwidth(r)
     uly = ulysses_measure(r) if not args.no_ulysses else {"skipped": "--no-ulysses"}
     lin = linear_measure(dev) if not args.no_linear else {"skipped": "--no-linear"}
-    others = (other_configs_measure(dev, w.name) if world == 1 and not args.no_other_configs
+    others = (other_configs_measure(dev, args.workload) if world == 1 and not args.no_other_configs
               else {"skipped": "--no-other-configs" if args.no_other_configs else "N > 1"})
 
     peaks, peak_kind = load_peaks()
@@ -788,7 +812,7 @@ def run_reference(args):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return None
-    w = workloads.get(args.workload)
+    w = chosen_workload(args)
     vals = []
     for _ in range(args.warmup):
         oracle_sample(w, args.cpu_tokens // 2)
@@ -827,6 +851,10 @@ def main():
                     help="skip the throughput lines of the other standard problems")
     ap.add_argument("--layout", default=None, choices=["contiguous", "zigzag", "striped"],
                     help="shard layout instead of the workload's own (zigzag for the standard ones)")
+    ap.add_argument("--seq-len", type=int, default=None, help="sequence length (single-sequence workloads)")
+    ap.add_argument("--heads", default=None, help="query:key-value head counts, e.g. 32:8")
+    ap.add_argument("--cp-size", type=int, default=None, help="number of context-parallel shards C")
+    ap.add_argument("--seed", type=int, default=None, help="input generator seed")
     args = ap.parse_args()
     if args.impl == "reference":
         res = run_reference(args)

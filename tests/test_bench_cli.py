@@ -39,3 +39,21 @@ def test_gpu_arm_fails_without_cuda():
     p = _run(["--steps", "1", "--warmup", "0", "--no-cpu-baseline", "--no-ulysses", "--no-linear"])
     assert p.returncode != 0
     assert not any(l.startswith("{") for l in p.stdout.splitlines())
+
+
+def test_reference_arm_takes_the_overrides():
+    p = _run(["--impl", "reference", "--steps", "1", "--warmup", "0", "--cpu-tokens", "256", "--cp-size", "4",
+              "--heads", "16:4", "--seq-len", "32768", "--seed", "3"])
+    assert p.returncode == 0, p.stderr[-2000:]
+    d = json.loads([l for l in p.stdout.splitlines() if l.startswith("{")][0])
+    c = d["config"]
+    assert (c["total_tokens"], c["hq"], c["hkv"], c["cp_size"]) == (32768, 16, 4, 4)
+    assert c["workload"].startswith("bf16_gqa_s64k_h32kv8_d128_c8_zigzag[")
+
+
+def test_bad_override_is_refused():
+    p = _run(["--impl", "reference", "--steps", "1", "--warmup", "0", "--heads", "6:4"])
+    assert p.returncode != 0
+    p = _run(["--impl", "reference", "--steps", "1", "--warmup", "0", "--workload",
+              "bf16_varlen_t128k_h16kv4_d128_c16_zigzag", "--seq-len", "1024"])
+    assert p.returncode != 0
