@@ -30,10 +30,11 @@
 // attn_bwd_dq_kernel — query-tile-major.  One CTA owns a 128-row query tile
 //   of one head and visits the key tiles of the forward plan; dQ accumulates
 //   in TMEM over all of them and is written once.  Per step:
-//     [0,128)   S = Q K^T (SS)
+//     [0,128)   S = Q K^T (TS with Q in TMEM for 128-wide heads, else SS)
 //     [128,256) dP = dO V^T (SS)
 //     [256,256+DQK) dQ += dS K (TS)
-//     then 64 columns per dS buffer (bf16; two buffers when they fit)
+//     then 64 columns of dS (bf16; one buffer: a second one measured no
+//     faster), then Q (bf16, 128-wide heads)
 //   S(j+1) is issued as soon as S(j) has been read and dP(j+1) as soon as
 //   dP(j) has been read, ahead of dQ(j).
 //
