@@ -63,3 +63,31 @@ def test_forward_backward_bit_identical_across_runs(case):
     names = ("o", "lse", "dq", "dk", "dv", "ring o", "ring lse")
     for name, a, b in zip(names, runs[0], runs[1]):
         assert torch.equal(a, b), name
+
+
+def test_ulysses_and_linear_attention_bit_identical_across_runs():
+    """The all-to-all path (re-layout kernels around the same attention
+    kernels) and the decayed linear attention (chunk states, a fixed-order
+    prefix over chunks, then the chunk outputs) are deterministic as well."""
+    w = workloads.Workload(name="det", dtype="bf16", seed=67, total_tokens=5000, hq=8, hkv=4, d_qk=128, d_v=128,
+                           cp_size=4, layout="zigzag", seqlens=(2100, 9, 2891))
+    inp = workloads.make_inputs(w, device="cuda", with_dout=True)
+    cu = inp["cu_seqlens"].tolist()
+    prob = cpa.Problem(w.total_tokens, w.hq, w.hkv, w.d_qk, w.d_v, w.cp_size, w.layout, cu)
+    sh = {n: cpa.cp_shard_permute(prob, inp[n]) for n in ("q", "k", "v", "dout")}
+    lin = cpa.Problem(w.total_tokens, w.hq, w.hq, 128, 128, w.cp_size, "contiguous", cu, True, 128 ** -0.5,
+                      "blocked", torch.bfloat16)
+    gen = torch.Generator().manual_seed(67)
+    kl = (torch.randn(w.total_tokens, w.hq, 128, generator=gen) * 0.5).to(torch.bfloat16).cuda()
+    g = (-torch.rand(w.hq, generator=gen) * 0.9 - 0.05).cuda()
+    ql = inp["q"]
+    runs = []
+    for _ in range(2):
+        o, lse = cpa.cp_ulysses_attn_fwd(prob, sh["q"], sh["k"], sh["v"])
+        dq, dk, dv = cpa.cp_ulysses_attn_bwd(prob, sh["q"], sh["k"], sh["v"], o, lse, sh["dout"])
+        o_lin = cpa.cp_lin_attn_fwd(lin, ql, kl, ql, g)
+        runs.append((o, lse, dq, dk, dv, o_lin))
+    torch.cuda.synchronize()
+    assert cpa.cp_device_status() == 0
+    for name, a, b in zip(("o", "lse", "dq", "dk", "dv", "linear o"), runs[0], runs[1]):
+        assert torch.equal(a, b), name
