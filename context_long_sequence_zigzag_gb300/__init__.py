@@ -11,7 +11,7 @@ a non-OK status.
 
 Functions carry the C names: ``cp_shard_permute``, ``cp_attn_block_fwd``,
 ``cp_lse_merge``, ``cp_attn_fwd``, ``cp_attn_bwd``, ``cp_workspace_size``,
-``cp_shard_offsets``, ``cp_rank_block_counts``, ``cp_device_status``,
+``cp_shard_offsets``, ``cp_rank_block_counts``, ``cp_rank_fwd_key_tiles``, ``cp_device_status``,
 ``cp_check_bounded_wait``, ``cp_status_string``, ``cp_validate``, ``cp_ulysses_a2a``,
 ``cp_ulysses_attn_fwd``, ``cp_ulysses_attn_bwd``, ``cp_ring_attn_fwd``, ``cp_lin_attn_fwd``.
 """
@@ -44,7 +44,7 @@ CP_OP_ULYSSES_A2A, CP_OP_ULYSSES_FWD, CP_OP_ULYSSES_BWD, CP_OP_LIN_FWD, CP_OP_RI
 
 EXPORTED = [
     "cp_status_string", "cp_validate", "cp_workspace_size", "cp_shard_offsets",
-    "cp_rank_block_counts", "cp_shard_permute", "cp_attn_block_fwd", "cp_lse_merge",
+    "cp_rank_block_counts", "cp_rank_fwd_key_tiles", "cp_shard_permute", "cp_attn_block_fwd", "cp_lse_merge",
     "cp_attn_fwd", "cp_attn_bwd", "cp_device_status", "cp_check_bounded_wait",
     "cp_attn_fwd_noalloc", "cp_attn_bwd_prep", "cp_attn_bwd_dkdv", "cp_attn_bwd_dq",
     "cp_ulysses_a2a", "cp_ulysses_attn_fwd", "cp_ulysses_attn_bwd", "cp_lin_attn_fwd", "cp_ring_attn_fwd",
@@ -78,6 +78,7 @@ _sigs = {
     "cp_workspace_size": (ctypes.c_int, [_DP, ctypes.c_int32, ctypes.POINTER(ctypes.c_size_t)]),
     "cp_shard_offsets": (ctypes.c_int, [_DP, ctypes.POINTER(ctypes.c_int64)]),
     "cp_rank_block_counts": (ctypes.c_int, [_DP, ctypes.POINTER(ctypes.c_int64)]),
+    "cp_rank_fwd_key_tiles": (ctypes.c_int, [_DP, ctypes.POINTER(ctypes.c_int64)]),
     "cp_shard_permute": (ctypes.c_int, [_DP, _P, _P, ctypes.c_int64, ctypes.c_int32, _P, ctypes.c_size_t, _P]),
     "cp_attn_block_fwd": (ctypes.c_int, [_DP, ctypes.c_int32, ctypes.c_int32, _P, _P, _P, _P, _P, _P,
                                          ctypes.c_size_t, _P]),
@@ -203,6 +204,12 @@ def cp_shard_offsets(prob: Problem) -> list:
 def cp_rank_block_counts(prob: Problem) -> list:
     arr = (ctypes.c_int64 * prob.desc.cp_size)()
     _check(_lib.cp_rank_block_counts(prob.ptr, arr), "cp_rank_block_counts")
+    return list(arr)
+
+
+def cp_rank_fwd_key_tiles(prob: Problem) -> list:
+    arr = (ctypes.c_int64 * prob.desc.cp_size)()
+    _check(_lib.cp_rank_fwd_key_tiles(prob.ptr, arr), "cp_rank_fwd_key_tiles")
     return list(arr)
 
 

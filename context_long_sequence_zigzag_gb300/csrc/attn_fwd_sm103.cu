@@ -32,7 +32,8 @@
 //              moves by more than 2^8, and finally normalises O and writes
 //              o / lse.
 //   warp 4     TMA producers: lane 0 loads Q, then streams K; lane 1 streams
-//              V, each into its own ring.
+//              V, each into its own ring.  A gathered key tile (a plan
+//              run of kind kRangePacked) arrives as one box per piece.
 //   warp 5     TMEM allocator; issues S(j) = Q K(j)^T.
 //   warp 6     issues O += P(j) V(j).
 #include <cuda.h>
@@ -75,7 +76,12 @@ struct FwdCfg {
   static constexpr uint32_t offV = offK + NSK * kKBytes;
   static constexpr uint32_t offBar = offV + NSV * kVBytes;
   static constexpr int kNumBars = 1 + 2 * NSK + 2 * NSV + 3 * NS_S + 2;
-  static constexpr uint32_t kSmem = offBar + kNumBars * 8 + 16;
+  // the tile's runs and the key masks of its gathered tiles, staged for the
+  // softmax warps when the tile has at most kSlots runs
+  static constexpr int kSlots = 64;
+  static constexpr uint32_t offRanges = (offBar + kNumBars * 8 + 16 + 15) / 16 * 16;
+  static constexpr uint32_t offMasks = offRanges + kSlots * 16;
+  static constexpr uint32_t kSmem = offMasks + kSlots * 16;
   // TMEM columns
   static constexpr uint32_t tS0 = 0;
   static constexpr uint32_t tO = NS_S * BN;
@@ -84,8 +90,16 @@ struct FwdCfg {
   static_assert(kSmem <= 232448, "shared memory budget");
 };
 
+// Boxes of 8, 16, ..., 120 rows of K and V for the pieces of gathered key
+// tiles (kRangePacked runs): a piece of r rows (a multiple of 8) is one box
+// per panel (map r / 8 - 1; the 128-row maps for r = 128).  One box per piece
+// matters: loading a piece as several boxes of 64, 32, 16 and 8 rows made the
+// forward on a 128K-token pack of short sequences 9 % slower.
+constexpr int kPieceMaps = 15;
+
 struct FwdParams {
   CUtensorMap tq, tk, tv;
+  CUtensorMap tkp[kPieceMaps], tvp[kPieceMaps];  // box rows 8 (i + 1)
   AttnArgs a;
   int32_t* err;
 };
@@ -102,7 +116,9 @@ struct KvCursor {
     off = 0;
     if (count > 0) cur = r[0];
   }
-  // Current tile: first row, rows, position of the first row.
+  // Current tile: first row, rows, position of the first row; a gathered
+  // tile (packed()) has its pieces from entry row0 and its key mask at pos0.
+  __device__ bool packed() const { return (cur.flags & kRangePacked) != 0; }
   __device__ int row() const { return cur.row0 + off; }
   __device__ int n() const { return min(BN, cur.nrows - off); }
   __device__ int pos() const { return cur.pos0 + off; }
@@ -136,7 +152,10 @@ __device__ __forceinline__ int head_of_slot(int slot, const AttnArgs& a) {
   return a.gqa_interleaved ? g * a.hkv + kv : kv * G + g;
 }
 
-template <int DQK, int DV>
+// PACKED: the plan has gathered key tiles (kRangePacked runs).  Plans without
+// them run an instantiation without that code: the extra branches slowed the
+// S = 64K forward by 2-3 % where they never ran.
+template <int DQK, int DV, bool PACKED>
 __global__ void __launch_bounds__(224, 1) attn_fwd_tc_kernel(const __grid_constant__ FwdParams p) {
   using Cfg = FwdCfg<DQK, DV>;
   extern __shared__ __align__(1024) uint8_t smem[];
@@ -203,6 +222,8 @@ __global__ void __launch_bounds__(224, 1) attn_fwd_tc_kernel(const __grid_consta
     ptx::prefetch_tmap(&p.tk);
     ptx::prefetch_tmap(&p.tv);
   }
+  if (PACKED && warp == 4 && lane >= 2)  // the piece maps, one per lane
+    ptx::prefetch_tmap(lane < 2 + kPieceMaps ? &p.tkp[lane - 2] : &p.tvp[lane - 2 - kPieceMaps]);
   ptx::tc_fence_before();
   __syncthreads();
   ptx::tc_fence_after();
@@ -235,8 +256,22 @@ __global__ void __launch_bounds__(224, 1) attn_fwd_tc_kernel(const __grid_consta
         const int st = j % NS;
         if (j >= NS && !ptx::mbar_wait(empty(st), ((j / NS) - 1) & 1, kstream ? kSiteKEmpty : kSiteVEmpty, wctx)) break;
         ptx::mbar_arrive_expect_tx(full(st), bytes);
-        for (int c = 0; c < panels; ++c)
-          ptx::tma_load_3d(base + st * bytes + c * kSubTile, map, full(st), c * 64, kvh, cur.row());
+        if (!PACKED || !cur.packed()) {
+          for (int c = 0; c < panels; ++c)
+            ptx::tma_load_3d(base + st * bytes + c * kSubTile, map, full(st), c * 64, kvh, cur.row());
+        } else {
+          // the pieces cover tile rows [0, BN) from 8-row (1 KiB) boundaries,
+          // so the boxes land on whole swizzle atoms and fill every row
+          const CUtensorMap* maps = kstream ? p.tkp : p.tvp;
+          const int count = cur.cur.flags >> kPackCountShift;
+          for (int i = 0; i < count; ++i) {
+            const PackPiece pc = a.pieces[cur.cur.row0 + i];
+            const CUtensorMap* m = pc.rows >= BN ? map : maps + (max(pc.rows, 8) >> 3) - 1;
+            for (int c = 0; c < panels; ++c)
+              ptx::tma_load_3d(base + st * bytes + c * kSubTile + uint32_t(pc.dst) * 128, m, full(st), c * 64, kvh,
+                               pc.src);
+          }
+        }
         ++issued;
       }
       if (*abort_flag) {
@@ -318,8 +353,23 @@ __global__ void __launch_bounds__(224, 1) attn_fwd_tc_kernel(const __grid_consta
     // A warp whose 32 rows all lie past a ragged tile only keeps the barrier
     // phases: P of those TMEM lanes feeds only O rows that are never stored.
     const bool idle_warp = __all_sync(0xffffffffu, !row_ok);
+    // The tile's runs, and the key masks of its gathered tiles, are staged
+    // in shared memory once, so that stepping from one short run to the next
+    // costs no global-memory round trip on the softmax's critical path.
+    RangeDesc* rtab = reinterpret_cast<RangeDesc*>(smem + Cfg::offRanges);
+    uint4* mtab = reinterpret_cast<uint4*>(smem + Cfg::offMasks);
+    const bool staged = PACKED && tile.range_count <= Cfg::kSlots;  // the same for the whole CTA
+    if (staged) {
+      for (int i = row; i < tile.range_count; i += 128) {
+        const RangeDesc r = a.ranges[tile.range_begin + i];
+        rtab[i] = r;
+        if (r.flags & kRangePacked) mtab[i] = *reinterpret_cast<const uint4*>(a.packs[r.pos0].valid);
+      }
+      ptx::named_barrier(1, 128);  // the four softmax warps, before any wait
+    }
     KvCursor cur;
-    cur.init(a.ranges, tile.range_begin, tile.range_count);
+    if (staged) cur.init(rtab, 0, tile.range_count);
+    else cur.init(a.ranges, tile.range_begin, tile.range_count);
     for (int j = 0; j < n_kv; ++j, cur.next()) {
       const int sb = j % Cfg::NS_S;
       const uint32_t tS = tmem + lane_base + Cfg::tS0 + BN * sb;
@@ -341,16 +391,39 @@ __global__ void __launch_bounds__(224, 1) attn_fwd_tc_kernel(const __grid_consta
 #pragma unroll
       for (int c = 0; c < 4; ++c) ptx::reg_fence32(sr[c]);
 
-      // mask: columns at or beyond `lim` are not visible to this row
+      // mask: columns at or beyond `lim` are not visible to this row, nor,
+      // in a gathered key tile, the columns that hold no key
+      const bool packed = PACKED && cur.packed();
       const int kn = cur.n(), kp = cur.pos();
       int lim = row_ok ? kn : 0;
-      if (a.causal) lim = min(lim, qpos - kp + 1);
-      if (lim < BN) {
+      if (a.causal && !packed) lim = min(lim, qpos - kp + 1);
+      if (!PACKED) {
+        if (lim < BN) {
+#pragma unroll
+          for (int c = 0; c < 4; ++c)
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+              if (c * 32 + i >= lim) sr[c][i] = __float_as_uint(-INFINITY);
+        }
+      } else if (lim < BN || packed) {
+        uint32_t vm[4] = {0xffffffffu, 0xffffffffu, 0xffffffffu, 0xffffffffu};
+        if (packed) {
+          const uint4 vk = staged ? mtab[cur.ri] : *reinterpret_cast<const uint4*>(a.packs[cur.cur.pos0].valid);
+          vm[0] = vk.x;
+          vm[1] = vk.y;
+          vm[2] = vk.z;
+          vm[3] = vk.w;
+        }
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {  // and the columns below lim
+          const int t = lim - 32 * c;
+          vm[c] &= t >= 32 ? 0xffffffffu : (t <= 0 ? 0u : (1u << t) - 1u);
+        }
 #pragma unroll
         for (int c = 0; c < 4; ++c)
 #pragma unroll
           for (int i = 0; i < 32; ++i)
-            if (c * 32 + i >= lim) sr[c][i] = __float_as_uint(-INFINITY);
+            if (!(vm[c] & (1u << i))) sr[c][i] = __float_as_uint(-INFINITY);
       }
       // P = exp2(s * scale * log2e - mref) (bf16, two per column) over the
       // first half of the S buffer (PV(j-3) finished reading it before S(j)
@@ -571,12 +644,20 @@ static cudaError_t launch_fwd_impl(const AttnArgs& a, cudaStream_t st) {
       !make_map_3d(&p.tv, a.v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, DV, a.hkv, a.T_kv ? a.T_kv : a.T, 64, BN,
                    CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
-  cudaError_t e = cudaFuncSetAttribute(attn_fwd_tc_kernel<DQK, DV>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       int(Cfg::kSmem));
+  if (a.num_packs > 0) {
+    for (int m = 0; m < kPieceMaps; ++m)
+      if (!make_map_3d(&p.tkp[m], a.k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, DQK, a.hkv, a.T_kv ? a.T_kv : a.T, 64,
+                       8 * (m + 1), CU_TENSOR_MAP_SWIZZLE_128B) ||
+          !make_map_3d(&p.tvp[m], a.v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, DV, a.hkv, a.T_kv ? a.T_kv : a.T, 64,
+                       8 * (m + 1), CU_TENSOR_MAP_SWIZZLE_128B))
+        return cudaErrorInvalidValue;
+  }
+  auto kernel = a.num_packs > 0 ? attn_fwd_tc_kernel<DQK, DV, true> : attn_fwd_tc_kernel<DQK, DV, false>;
+  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(Cfg::kSmem));
   if (e != cudaSuccess) return e;
   const int64_t grid = int64_t(a.num_tiles) * a.hq;
   if (grid == 0) return cudaSuccess;
-  attn_fwd_tc_kernel<DQK, DV><<<unsigned(grid), 224, Cfg::kSmem, st>>>(p);
+  kernel<<<unsigned(grid), 224, Cfg::kSmem, st>>>(p);
   return cudaGetLastError();
 }
 

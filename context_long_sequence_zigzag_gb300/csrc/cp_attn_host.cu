@@ -185,8 +185,70 @@ bool merge_ok(const ShardMap& m, int seq) {
 struct Plan {
   std::vector<TileDesc> tiles;
   std::vector<RangeDesc> ranges;
+  std::vector<PackMask> packs;  // key masks of the gathered key tiles (kRangePacked runs)
+  std::vector<PackPiece> pieces;
   int32_t max_ranges = 0;
 };
+
+int32_t round8(int32_t n) { return (n + 7) & ~7; }
+
+// Gathers the ragged tails of a query tile's unmasked runs into shared key
+// tiles.  Every key of an unmasked run is visible to every row of the tile,
+// so where a key sits in the tile does not matter: each run keeps its whole
+// kTile-row steps as a run of its own, and the tails (fewer than kTile rows
+// each) are laid back to back from 8-row boundaries, split across two tiles
+// where one fills up.  The rows between a tail's last key and the next
+// boundary, and after the last tail up to the tile's end, are loaded from
+// the rows that follow it and masked.  Done only where it saves key tiles:
+// where the tails would need as many tiles gathered as apart, nothing changes.  Returns the tile's runs
+// (masked runs first, as built, then the whole steps, then the gathered
+// tiles) in place of [first, end) of p.ranges.
+void pack_tails(Plan& p, size_t first) {
+  std::vector<RangeDesc> keep;
+  std::vector<std::pair<int32_t, int32_t>> tails;  // (first sharded row, rows)
+  for (size_t i = first; i < p.ranges.size(); ++i) {
+    const RangeDesc r = p.ranges[i];
+    if (r.flags != 0 || r.nrows % kTile == 0) {
+      keep.push_back(r);
+      continue;
+    }
+    const int32_t whole = r.nrows - r.nrows % kTile;
+    if (whole > 0) keep.push_back(RangeDesc{r.row0, whole, r.pos0, 0});
+    tails.emplace_back(r.row0 + whole, r.nrows - whole);
+  }
+  int32_t rows = 0;
+  for (const auto& tl : tails) rows += round8(tl.second);
+  if ((rows + kTile - 1) / kTile >= int32_t(tails.size())) return;  // no key tile saved
+  p.ranges.resize(first);
+  p.ranges.insert(p.ranges.end(), keep.begin(), keep.end());
+  PackMask pk{};
+  int32_t dst = 0, piece0 = 0, count = 0;
+  auto close = [&]() {
+    PackPiece& last = p.pieces.back();
+    last.rows = kTile - last.dst;  // fill the tile with the rows that follow
+    p.ranges.push_back(RangeDesc{piece0, kTile, int32_t(p.packs.size()), kRangePacked | (count << kPackCountShift)});
+    p.packs.push_back(pk);
+    dst = 0;
+  };
+  for (auto [src, n] : tails) {
+    while (n > 0) {
+      if (dst == 0) {
+        pk = PackMask{};
+        piece0 = int32_t(p.pieces.size());
+        count = 0;
+      }
+      const int32_t take = std::min(n, kTile - dst);
+      p.pieces.push_back(PackPiece{src, dst, round8(take), take});
+      for (int32_t j = dst; j < dst + take; ++j) pk.valid[j >> 5] |= 1u << (j & 31);
+      ++count;
+      dst += round8(take);
+      src += take;
+      n -= take;
+      if (dst == kTile) close();
+    }
+  }
+  if (dst > 0) close();
+}
 
 int32_t ceil_tiles(int64_t n) { return int32_t((n + kTile - 1) / kTile); }
 
@@ -198,7 +260,7 @@ int32_t ceil_tiles(int64_t n) { return int32_t((n + kTile - 1) / kTile); }
 // sits in the holder's slot of a ring buffer whose rank slots are slot_rows
 // rows apart, and tiles that see nothing of it are left out.
 Plan build_fwd_plan(const cp_desc_t* d, const ShardMap& m, int q_rank, int kv_rank, int ring_step = -1,
-                    int64_t slot_rows = 0) {
+                    int64_t slot_rows = 0, bool pack = false) {
   Plan p;
   const bool causal = d->causal != 0;
   for (const Chunk& A : m.chunks) {
@@ -248,6 +310,11 @@ Plan build_fwd_plan(const cp_desc_t* d, const ShardMap& m, int q_rank, int kv_ra
           p.ranges.pop_back();
         }
         for (size_t i = first; i < p.ranges.size(); ++i) work += ceil_tiles(p.ranges[i].nrows);
+      }
+      if (pack) {
+        pack_tails(p, size_t(t.range_begin));
+        work = 0;
+        for (size_t i = size_t(t.range_begin); i < p.ranges.size(); ++i) work += ceil_tiles(p.ranges[i].nrows);
       }
       t.range_count = int32_t(p.ranges.size()) - t.range_begin;
       t.work = work;
@@ -329,7 +396,8 @@ void order_by_work(Plan& p) {
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 size_t plan_bytes(const Plan& p) {
-  return align256(p.tiles.size() * sizeof(TileDesc)) + align256(p.ranges.size() * sizeof(RangeDesc));
+  return align256(p.tiles.size() * sizeof(TileDesc)) + align256(p.ranges.size() * sizeof(RangeDesc)) +
+         align256(p.packs.size() * sizeof(PackMask)) + align256(p.pieces.size() * sizeof(PackPiece));
 }
 
 // Recently built plans.  A plan depends only on the shard map (T, the
@@ -338,7 +406,9 @@ size_t plan_bytes(const Plan& p) {
 // of rebuilding it on the host; the upload into the call's workspace still
 // happens every call, since the caller may use that memory for anything in
 // between.
-enum PlanKind : int64_t { kPlanQueryMajor = 0, kPlanKeyMajor = 1 };
+// kPlanQueryMajorPacked: the query-major plan with the unmasked runs' tails
+// gathered into shared key tiles (the tensor-core forward reads those).
+enum PlanKind : int64_t { kPlanQueryMajor = 0, kPlanKeyMajor = 1, kPlanQueryMajorPacked = 2 };
 std::shared_ptr<const Plan> get_plan(const cp_desc_t* d, const ShardMap& m, PlanKind kind, int q_rank = -1,
                                      int kv_rank = -1, int ring_step = -1, int64_t slot_rows = 0) {
   static std::mutex mu;
@@ -357,8 +427,10 @@ std::shared_ptr<const Plan> get_plan(const cp_desc_t* d, const ShardMap& m, Plan
         return it->second;
       }
   }
-  auto plan = std::make_shared<Plan>(kind == kPlanKeyMajor ? build_bwd_plan(d, m)
-                                                           : build_fwd_plan(d, m, q_rank, kv_rank, ring_step, slot_rows));
+  auto plan = std::make_shared<Plan>(kind == kPlanKeyMajor
+                                         ? build_bwd_plan(d, m)
+                                         : build_fwd_plan(d, m, q_rank, kv_rank, ring_step, slot_rows,
+                                                          kind == kPlanQueryMajorPacked));
   order_by_work(*plan);
   std::lock_guard<std::mutex> lock(mu);
   cache.emplace_front(std::move(key), plan);
@@ -482,22 +554,28 @@ cudaError_t h2d_async(void* dst, const void* src, size_t bytes, cudaStream_t st,
   return cudaMemcpyAsync(dst, src, bytes, cudaMemcpyHostToDevice, st);
 }
 
-// Copies the plan into the workspace at `base`; returns the device pointers.
-cudaError_t upload_plan(const Plan& p, char* base, cudaStream_t st, const TileDesc** tiles,
-                        const RangeDesc** ranges, bool pinned = true) {
+// Copies the plan into the workspace at `base` (tiles, runs, gathered key
+// tiles, their pieces, each from a 256-byte boundary) and points the kernel
+// arguments at it.
+cudaError_t upload_plan(const Plan& p, char* base, cudaStream_t st, AttnArgs& a, bool pinned = true) {
   const size_t tb = p.tiles.size() * sizeof(TileDesc);
   const size_t rb = p.ranges.size() * sizeof(RangeDesc);
+  const size_t kb = p.packs.size() * sizeof(PackMask);
+  const size_t pb = p.pieces.size() * sizeof(PackPiece);
   char* rbase = base + align256(tb);
-  if (tb) {
-    cudaError_t e = h2d_async(base, p.tiles.data(), tb, st, pinned);
+  char* kbase = rbase + align256(rb);
+  char* pbase = kbase + align256(kb);
+  const std::pair<char*, std::pair<const void*, size_t>> parts[] = {
+      {base, {p.tiles.data(), tb}}, {rbase, {p.ranges.data(), rb}}, {kbase, {p.packs.data(), kb}},
+      {pbase, {p.pieces.data(), pb}}};
+  for (const auto& part : parts) {
+    const cudaError_t e = h2d_async(part.first, part.second.first, part.second.second, st, pinned);
     if (e != cudaSuccess) return e;
   }
-  if (rb) {
-    cudaError_t e = h2d_async(rbase, p.ranges.data(), rb, st, pinned);
-    if (e != cudaSuccess) return e;
-  }
-  *tiles = reinterpret_cast<const TileDesc*>(base);
-  *ranges = reinterpret_cast<const RangeDesc*>(rbase);
+  a.tiles = reinterpret_cast<const TileDesc*>(base);
+  a.ranges = reinterpret_cast<const RangeDesc*>(rbase);
+  a.packs = kb ? reinterpret_cast<const PackMask*>(kbase) : nullptr;
+  a.pieces = pb ? reinterpret_cast<const PackPiece*>(pbase) : nullptr;
   return cudaSuccess;
 }
 
@@ -513,13 +591,16 @@ cp_status_t stage_plan(const Plan& p, char* base, cudaStream_t st, AttnArgs& a, 
                        int64_t range_rows, bool pinned = true) {
   if (a.debug) {
     for (int32_t i = 0; i < int32_t(p.tiles.size()); ++i)
-      if (plan_entry_check(p.tiles.data(), int32_t(p.tiles.size()), p.ranges.data(), int32_t(p.ranges.size()), i, 0,
-                           1, 0, 1, tile_rows, range_rows, a.block_mode, a.lse_stride) != 0)
+      if (plan_entry_check(p.tiles.data(), int32_t(p.tiles.size()), p.ranges.data(), int32_t(p.ranges.size()),
+                           p.packs.data(), int32_t(p.packs.size()), p.pieces.data(), int32_t(p.pieces.size()), i,
+                           0, 1, 0, 1, tile_rows, range_rows, a.block_mode, a.lse_stride) != 0)
         return CP_ERR_INVALID_ARG;
   }
-  if (upload_plan(p, base, st, &a.tiles, &a.ranges, pinned) != cudaSuccess) return CP_ERR_CUDA;
+  if (upload_plan(p, base, st, a, pinned) != cudaSuccess) return CP_ERR_CUDA;
   a.num_tiles = int32_t(p.tiles.size());
   a.num_ranges = int32_t(p.ranges.size());
+  a.num_packs = int32_t(p.packs.size());
+  a.num_pieces = int32_t(p.pieces.size());
   a.max_ranges = p.max_ranges;
   return CP_OK;
 }
@@ -532,6 +613,8 @@ bool use_tc_fwd(const cp_desc_t* d) {
 bool use_tc_bwd(const cp_desc_t* d) {
   return d->dtype == CP_DT_BF16 && tc_bwd_supported(d->d_qk, d->d_v);
 }
+// The whole forward's plan: the tensor-core kernel reads gathered key tiles.
+PlanKind fwd_plan_kind(const cp_desc_t* d) { return use_tc_fwd(d) ? kPlanQueryMajorPacked : kPlanQueryMajor; }
 
 AttnArgs base_args(const cp_desc_t* d) {
   AttnArgs a{};
@@ -870,7 +953,7 @@ cp_status_t cp_workspace_size(const cp_desc_t* d, int32_t op, size_t* bytes) {
   if (st != CP_OK) return st;
   ShardMap m = build_map(d);
   if (op == CP_OP_FWD) {
-    *bytes = plan_bytes(*get_plan(d, m, kPlanQueryMajor));
+    *bytes = plan_bytes(*get_plan(d, m, fwd_plan_kind(d)));
   } else if (op == CP_OP_BLOCK_FWD) {
     // the largest (q rank, kv rank) plan is bounded by the plan of rank q's
     // tiles against all ranks; size for the worst rank
@@ -914,6 +997,17 @@ cp_status_t cp_rank_block_counts(const cp_desc_t* d, int64_t* counts) {
   const Plan& p = *pp;
   for (int r = 0; r < m.C; ++r) counts[r] = 0;
   for (const TileDesc& t : p.tiles) counts[t.rank] += t.work;
+  return CP_OK;
+}
+
+cp_status_t cp_rank_fwd_key_tiles(const cp_desc_t* d, int64_t* counts) {
+  cp_status_t st = check_attn_fields(d);
+  if (st != CP_OK) return st;
+  if (counts == nullptr) return CP_ERR_INVALID_ARG;
+  ShardMap m = build_map(d);
+  const auto pp = get_plan(d, m, fwd_plan_kind(d));
+  for (int r = 0; r < m.C; ++r) counts[r] = 0;
+  for (const TileDesc& t : pp->tiles) counts[t.rank] += t.work;
   return CP_OK;
 }
 
@@ -1023,7 +1117,7 @@ cp_status_t cp_attn_fwd(const cp_desc_t* d, const void* q, const void* k, const 
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
     return CP_ERR_INVALID_ARG;
   ShardMap m = build_map(d);
-  const auto pp = get_plan(d, m, kPlanQueryMajor);
+  const auto pp = get_plan(d, m, fwd_plan_kind(d));
   const Plan& p = *pp;
   if (ws == nullptr || (reinterpret_cast<uintptr_t>(ws) & 255) || ws_bytes < plan_bytes(p))
     return CP_ERR_WORKSPACE;
@@ -1126,7 +1220,7 @@ cp_status_t cp_attn_fwd_noalloc(const cp_desc_t* d, const void* q, const void* k
   if (st != CP_OK) return st;
   if (d->total_tokens == 0) return CP_OK;
   ShardMap m = build_map(d);
-  const auto pp = get_plan(d, m, kPlanQueryMajor);
+  const auto pp = get_plan(d, m, fwd_plan_kind(d));
   const Plan& p = *pp;
   if (plan_bytes(p) > CP_NOALLOC_SCRATCH_BYTES) return CP_ERR_WORKSPACE;
   if (!q || !k || !v || !o || !lse) return CP_ERR_INVALID_ARG;

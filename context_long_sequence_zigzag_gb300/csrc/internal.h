@@ -41,6 +41,30 @@ struct RangeDesc {
 static_assert(sizeof(RangeDesc) == 16, "RangeDesc layout");
 
 constexpr int32_t kRangeMasked = 1;
+// The run is one key tile gathered from pieces of several runs: row0 is its
+// first entry in the piece array, flags >> 8 the number of pieces (1 ..
+// kTile / 8), pos0 its entry in the key-mask array, nrows kTile.  Every key
+// in it is visible to every row of the query tile, so no causal test applies.
+// Only the tensor-core forward's own plan has them.
+constexpr int32_t kRangePacked = 2;
+constexpr int32_t kPackCountShift = 8;
+
+// A key tile gathered from the ragged tails of the unmasked runs that one
+// query tile sees (every key of such a run is visible to every row of the
+// tile, so its keys may sit anywhere in the tile).  Pieces start at tile rows
+// that are multiples of 8 and follow one another up to row kTile.
+struct PackMask {
+  uint32_t valid[4];  // bit j % 32 of word j / 32: tile row j holds a key
+};
+static_assert(sizeof(PackMask) == 16, "PackMask layout");
+
+struct PackPiece {
+  int32_t src;   // first sharded row loaded
+  int32_t dst;   // first tile row, a multiple of 8
+  int32_t rows;  // rows loaded: a multiple of 8, dst + rows <= kTile
+  int32_t keys;  // the first `keys` of them are keys (1 .. rows); the rest fill the tile, masked
+};
+static_assert(sizeof(PackPiece) == 16, "PackPiece layout");
 
 // One contiguous copy of the shard permutation (a chunk of one sequence).
 struct CopySeg {
@@ -69,8 +93,12 @@ struct AttnArgs {
   void* dv;
   const TileDesc* tiles;
   const RangeDesc* ranges;
+  const PackMask* packs;    // key masks of the gathered key tiles (kRangePacked runs), or null
+  const PackPiece* pieces;  // their pieces
   int32_t num_tiles;
   int32_t num_ranges;
+  int32_t num_packs;
+  int32_t num_pieces;
   int32_t max_ranges;  // longest range list of any tile
   int32_t debug;       // nonzero: every CTA checks its plan entry first (plan_check.cuh)
   int32_t* err;        // device error word (set by the launchers)

@@ -8,6 +8,7 @@ import re
 
 import numpy as np
 import pytest
+import torch
 
 import oracle
 import workloads
@@ -124,6 +125,60 @@ def test_rank_block_counts(layout):
     cu = workloads.make_cu_seqlens(lengths).tolist()
     p = _prob(total_tokens=cu[-1], cu_seqlens=cu, cp_size=4, layout=layout)
     assert cpa.cp_rank_block_counts(p) == _tile_pairs_oracle(cu, 4, layout)
+
+
+def _fwd_key_tiles_model(cu, C, layout):
+    """Key tiles of the tensor-core forward per rank: as _tile_pairs_oracle,
+    except that the tails (rows past the last whole 128-row step) of the
+    runs a query tile sees whole and unmasked are laid back to back from
+    8-row boundaries into shared key tiles, which are used where they are
+    fewer than the tails."""
+    n = C if layout == "contiguous" else 2 * C
+    counts = []
+    for r in range(C):
+        tot = 0
+        for s in range(len(cu) - 1):
+            L = cu[s + 1] - cu[s]
+            b = oracle.chunk_bounds(L, n)
+            for ca in oracle.rank_chunks(r, C, layout):
+                for t0 in range(b[ca], b[ca + 1], 128):
+                    qmax = min(t0 + 128, b[ca + 1]) - 1
+                    tails = []
+                    for rho in range(C):
+                        runs = []
+                        for cb in oracle.rank_chunks(rho, C, layout):
+                            lo, hi = b[cb], b[cb + 1]
+                            if hi <= lo or lo > qmax:
+                                continue
+                            runs.append((min(hi - lo, qmax - lo + 1), hi - 1 <= t0))
+                        if layout == "zigzag" and len(runs) == 2 and runs[0][1] and runs[1][1]:
+                            runs = [(runs[0][0] + runs[1][0], True)]
+                        for v, visible in runs:
+                            if visible and v % 128:
+                                tot += v // 128
+                                tails.append(v % 128)
+                            else:
+                                tot += -(-v // 128)
+                    gathered = -(-sum(-(-t // 8) * 8 for t in tails) // 128)
+                    tot += min(gathered, len(tails))
+        counts.append(tot)
+    return counts
+
+
+@pytest.mark.parametrize("layout", ["contiguous", "zigzag"])
+def test_forward_gathers_run_tails(layout):
+    lengths = workloads.varlen_lengths(20000, 64, 4000, 3)
+    cu = workloads.make_cu_seqlens(lengths).tolist()
+    p = _prob(total_tokens=cu[-1], cu_seqlens=cu, cp_size=4, layout=layout)
+    got = cpa.cp_rank_fwd_key_tiles(p)
+    assert got == _fwd_key_tiles_model(cu, 4, layout)
+    assert sum(got) < sum(cpa.cp_rank_block_counts(p))
+    # the CUDA-core forward (fp32) and dense shards whose runs are whole
+    # 128-row steps keep one key tile per step
+    f32 = _prob(total_tokens=cu[-1], cu_seqlens=cu, cp_size=4, layout=layout, dtype=torch.float32)
+    assert cpa.cp_rank_fwd_key_tiles(f32) == cpa.cp_rank_block_counts(f32)
+    dense = _prob(total_tokens=8192, cu_seqlens=[0, 8192], cp_size=4, layout=layout)
+    assert cpa.cp_rank_fwd_key_tiles(dense) == cpa.cp_rank_block_counts(dense)
 
 
 def _striped_tile_pairs(cu, C):
