@@ -76,8 +76,15 @@ enum WaitSite : int {
   kSiteDrain, kSiteAlign, kSiteStat, kSiteKVFull, kSiteKVEmpty, kSiteQ,
 };
 
+// Boxes of 8, 16, ..., 120 rows of K and V for the pieces of gathered key
+// tiles (kRangePacked runs of the dQ kernel's plan): a piece of r rows (a
+// multiple of 8) is one box per panel (map r / 8 - 1; the 128-row maps for
+// r = 128).
+constexpr int kPieceMaps = 15;
+
 struct BwdParams {
   CUtensorMap tq, tk, tv, tdo;
+  CUtensorMap tkp[kPieceMaps], tvp[kPieceMaps];  // box rows 8 (i + 1); dQ with gathered tiles only
   AttnArgs a;
   int32_t* err;
 };
@@ -596,6 +603,9 @@ struct KvCursor {
     off = 0;
     if (count > 0) cur = r[0];
   }
+  // a gathered tile (packed()) has its pieces from entry row0 and its key
+  // mask at pos0
+  __device__ bool packed() const { return (cur.flags & kRangePacked) != 0; }
   __device__ int row() const { return cur.row0 + off; }
   __device__ int n() const { return min(BT, cur.nrows - off); }
   __device__ int pos() const { return cur.pos0 + off; }
@@ -628,14 +638,21 @@ struct DqCfg {
   static constexpr uint32_t offV = offK + NSK * kKBytes;     // NSV stages
   static constexpr uint32_t offBar = offV + NSV * kVBytes;
   static constexpr int kNumBars = 1 + 2 * NSK + 2 * NSV + 9 + NB;
-  static constexpr uint32_t kSmem = offBar + kNumBars * 8 + 16;
+  // the tile's runs and the key masks of its gathered tiles, staged for the
+  // compute warps when the tile has at most kSlots runs (gathering plans only)
+  static constexpr int kSlots = 64;
+  static constexpr uint32_t offRanges = (offBar + kNumBars * 8 + 16 + 15) / 16 * 16;
+  static constexpr uint32_t offMasks = offRanges + kSlots * 16;
+  static constexpr uint32_t kSmem = offMasks + kSlots * 16;
   // TMEM columns
   static constexpr uint32_t tS = 0, tDP = 128, tDQ = 256, tDS = 256 + DQK, tQ = tDS + 64 * NB;
   static_assert(tQ + (kQTmem ? DQK / 2 : 0) <= 512, "TMEM budget");
   static_assert(kSmem <= 232448, "shared memory budget");
 };
 
-template <int DQK>
+// PACKED: the plan has gathered key tiles (kRangePacked runs); plans without
+// them run an instantiation without that code.
+template <int DQK, bool PACKED>
 __global__ void __launch_bounds__(kThreadsDq, 1) attn_bwd_dq_kernel(const __grid_constant__ BwdParams p) {
   using Cfg = DqCfg<DQK>;
   constexpr int NB = Cfg::NB;
@@ -707,6 +724,8 @@ __global__ void __launch_bounds__(kThreadsDq, 1) attn_bwd_dq_kernel(const __grid
     ptx::prefetch_tmap(&p.tv);
     ptx::prefetch_tmap(&p.tdo);
   }
+  if (PACKED && warp == 8 && lane >= 2)  // the piece maps, one per lane
+    ptx::prefetch_tmap(lane < 2 + kPieceMaps ? &p.tkp[lane - 2] : &p.tvp[lane - 2 - kPieceMaps]);
   ptx::tc_fence_before();
   __syncthreads();
   ptx::tc_fence_after();
@@ -741,8 +760,22 @@ __global__ void __launch_bounds__(kThreadsDq, 1) attn_bwd_dq_kernel(const __grid
         const int st = j % NS;
         if (j >= NS && !ptx::mbar_wait(empty(st), ((j / NS) - 1) & 1, kSiteKVEmpty, wctx)) break;
         ptx::mbar_arrive_expect_tx(full(st), bytes);
-        for (int c = 0; c < panels; ++c)
-          ptx::tma_load_3d(base + st * bytes + c * kPanel, map, full(st), c * 64, kvh, cur.row());
+        if (!PACKED || !cur.packed()) {
+          for (int c = 0; c < panels; ++c)
+            ptx::tma_load_3d(base + st * bytes + c * kPanel, map, full(st), c * 64, kvh, cur.row());
+        } else {
+          // one box per piece; the pieces cover tile rows [0, BT) from 8-row
+          // (1 KiB) boundaries
+          const CUtensorMap* maps = kstream ? p.tkp : p.tvp;
+          const int count = cur.cur.flags >> kPackCountShift;
+          for (int i = 0; i < count; ++i) {
+            const PackPiece pc = a.pieces[cur.cur.row0 + i];
+            const CUtensorMap* m = pc.rows >= BT ? map : maps + (max(pc.rows, 8) >> 3) - 1;
+            for (int c = 0; c < panels; ++c)
+              ptx::tma_load_3d(base + st * bytes + c * kPanel + uint32_t(pc.dst) * 128, m, full(st), c * 64, kvh,
+                               pc.src);
+          }
+        }
         ++issued;
       }
       if (*abort_flag) {
@@ -891,13 +924,29 @@ __global__ void __launch_bounds__(kThreadsDq, 1) attn_bwd_dq_kernel(const __grid
       if (lane == 0) ptx::mbar_arrive(bar_qt);
     }
     bool ok = true;
+    // With gathered tiles the runs and key masks are staged in shared memory
+    // once (the mask is needed on the P critical path).
+    RangeDesc* rtab = reinterpret_cast<RangeDesc*>(smem + Cfg::offRanges);
+    uint4* mtab = reinterpret_cast<uint4*>(smem + Cfg::offMasks);
+    const bool staged = PACKED && tile.range_count <= Cfg::kSlots;  // the same for the whole CTA
+    if (staged) {
+      for (int i = threadIdx.x; i < tile.range_count; i += kComputeThreads) {
+        const RangeDesc rd = a.ranges[tile.range_begin + i];
+        rtab[i] = rd;
+        if (rd.flags & kRangePacked) mtab[i] = *reinterpret_cast<const uint4*>(a.packs[rd.pos0].valid);
+      }
+      ptx::named_barrier(1, kComputeThreads);  // the eight compute warps, before any wait
+    }
     KvCursor cur;
-    cur.init(a.ranges, tile.range_begin, tile.range_count);
+    if (staged) cur.init(rtab, 0, tile.range_count);
+    else cur.init(a.ranges, tile.range_begin, tile.range_count);
     for (int j = 0; j < n_kv; ++j, cur.next()) {
+      const bool packed = PACKED && cur.packed();
       const int kn = cur.n(), kp = cur.pos();
-      const bool need_mask = kn < BT || tile.nrows < BT || (a.causal && kp + BT - 1 > tile.pos0);
+      const bool need_mask =
+          packed || kn < BT || tile.nrows < BT || (a.causal && kp + BT - 1 > tile.pos0);
       int lim = row_ok ? kn : 0;
-      if (a.causal) lim = min(lim, qpos - kp + 1);
+      if (a.causal && !packed) lim = min(lim, qpos - kp + 1);
       lim -= int(colS);  // columns [0, lim) of this group are visible
 
       // ---- P = exp(S * scale - lse)
@@ -910,7 +959,25 @@ __global__ void __launch_bounds__(kThreadsDq, 1) attn_bwd_dq_kernel(const __grid
       if (lane == 0) ptx::mbar_arrive(bar_p_full);  // S(j) has been read
       float pf[64];
       const float4 nl4 = make_float4(-lse2, -lse2, -lse2, -lse2);
-      if (need_mask) {  // warp-uniform: diagonal and ragged tiles only
+      if (PACKED && need_mask) {  // the group's 64 columns: below lim and, if gathered, holding a key
+        uint32_t vm[2];
+#pragma unroll
+        for (int w = 0; w < 2; ++w) {
+          const int t = lim - 32 * w;
+          vm[w] = t >= 32 ? 0xffffffffu : (t <= 0 ? 0u : (1u << t) - 1u);
+        }
+        if (packed) {
+          const uint4 vk = staged ? mtab[cur.ri] : *reinterpret_cast<const uint4*>(a.packs[cur.cur.pos0].valid);
+          vm[0] &= grp ? vk.z : vk.x;
+          vm[1] &= grp ? vk.w : vk.y;
+        }
+#pragma unroll
+        for (int c = 0; c < 64; c += 4) {
+          exp4<64>(x, c, sl2x2, nl4, pf + c);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) pf[c + e] = (vm[(c + e) >> 5] & (1u << ((c + e) & 31))) ? pf[c + e] : 0.f;
+        }
+      } else if (need_mask) {  // warp-uniform: diagonal and ragged tiles only
 #pragma unroll
         for (int c = 0; c < 64; c += 4) {
           exp4<64>(x, c, sl2x2, nl4, pf + c);
@@ -998,12 +1065,20 @@ cudaError_t launch_dq(const AttnArgs& a, cudaStream_t st) {
   p.a = a;
   p.err = device_error_word();
   if (!make_maps(p, a, DQK, BT)) return cudaErrorInvalidValue;
-  cudaError_t e = cudaFuncSetAttribute(attn_bwd_dq_kernel<DQK>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       int(Cfg::kSmem));
+  if (a.num_packs > 0) {
+    for (int m = 0; m < kPieceMaps; ++m)
+      if (!make_map_3d(&p.tkp[m], a.k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, DQK, a.hkv, a.T, 64, 8 * (m + 1),
+                       CU_TENSOR_MAP_SWIZZLE_128B) ||
+          !make_map_3d(&p.tvp[m], a.v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, DV, a.hkv, a.T, 64, 8 * (m + 1),
+                       CU_TENSOR_MAP_SWIZZLE_128B))
+        return cudaErrorInvalidValue;
+  }
+  auto kernel = a.num_packs > 0 ? attn_bwd_dq_kernel<DQK, true> : attn_bwd_dq_kernel<DQK, false>;
+  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(Cfg::kSmem));
   if (e != cudaSuccess) return e;
   const int64_t grid = int64_t(a.num_tiles) * a.hq;
   if (grid == 0) return cudaSuccess;
-  attn_bwd_dq_kernel<DQK><<<unsigned(grid), kThreadsDq, Cfg::kSmem, st>>>(p);
+  kernel<<<unsigned(grid), kThreadsDq, Cfg::kSmem, st>>>(p);
   return cudaGetLastError();
 }
 

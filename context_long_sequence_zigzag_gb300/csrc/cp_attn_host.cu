@@ -613,8 +613,10 @@ bool use_tc_fwd(const cp_desc_t* d) {
 bool use_tc_bwd(const cp_desc_t* d) {
   return d->dtype == CP_DT_BF16 && tc_bwd_supported(d->d_qk, d->d_v);
 }
-// The whole forward's plan: the tensor-core kernel reads gathered key tiles.
+// The whole forward's plan and the dQ kernel's: the tensor-core kernels read
+// gathered key tiles.
 PlanKind fwd_plan_kind(const cp_desc_t* d) { return use_tc_fwd(d) ? kPlanQueryMajorPacked : kPlanQueryMajor; }
+PlanKind dq_plan_kind(const cp_desc_t* d) { return use_tc_bwd(d) ? kPlanQueryMajorPacked : kPlanQueryMajor; }
 
 AttnArgs base_args(const cp_desc_t* d) {
   AttnArgs a{};
@@ -646,7 +648,7 @@ cp_status_t run_bwd_dkdv(const cp_desc_t* d, const ShardMap& m, AttnArgs a, char
 // Uploads the query-major plan into `ws` and launches the dQ kernel.
 cp_status_t run_bwd_dq(const cp_desc_t* d, const ShardMap& m, AttnArgs a, char* ws, size_t ws_bytes,
                        cudaStream_t cs) {
-  const auto pfp = get_plan(d, m, kPlanQueryMajor);
+  const auto pfp = get_plan(d, m, dq_plan_kind(d));
   const Plan& pf = *pfp;
   if (ws == nullptr || (reinterpret_cast<uintptr_t>(ws) & 255) || ws_bytes < plan_bytes(pf)) return CP_ERR_WORKSPACE;
   const cp_status_t st = stage_plan(pf, ws, cs, a, d->total_tokens, d->total_tokens);
@@ -961,11 +963,11 @@ cp_status_t cp_workspace_size(const cp_desc_t* d, int32_t op, size_t* bytes) {
     for (int r = 0; r < m.C; ++r) mx = std::max(mx, plan_bytes(build_fwd_plan(d, m, r, -1)));
     *bytes = mx;
   } else if (op == CP_OP_BWD) {
-    *bytes = bwd_layout(d, *get_plan(d, m, kPlanQueryMajor), *get_plan(d, m, kPlanKeyMajor)).total;
+    *bytes = bwd_layout(d, *get_plan(d, m, dq_plan_kind(d)), *get_plan(d, m, kPlanKeyMajor)).total;
   } else if (op == CP_OP_BWD_DKDV) {
     *bytes = plan_bytes(*get_plan(d, m, kPlanKeyMajor));
   } else if (op == CP_OP_BWD_DQ) {
-    *bytes = plan_bytes(*get_plan(d, m, kPlanQueryMajor));
+    *bytes = plan_bytes(*get_plan(d, m, dq_plan_kind(d)));
   } else if (op == CP_OP_RING_FWD) {
     *bytes = ring_layout(d, m).total;
   } else if (op == CP_OP_ULYSSES_FWD || op == CP_OP_ULYSSES_BWD) {
@@ -1145,7 +1147,7 @@ cp_status_t cp_attn_bwd(const cp_desc_t* d, const void* q, const void* k, const 
   for (const void* p : ptrs)
     if (p == nullptr || !aligned16(p)) return CP_ERR_INVALID_ARG;
   ShardMap m = build_map(d);
-  const auto pfp = get_plan(d, m, kPlanQueryMajor);
+  const auto pfp = get_plan(d, m, dq_plan_kind(d));
   const auto pbp = get_plan(d, m, kPlanKeyMajor);
   const Plan& pf = *pfp;
   const Plan& pb = *pbp;

@@ -140,15 +140,16 @@ cp_status_t cp_shard_offsets(const cp_desc_t* desc, int64_t* offsets);
  * array of C int64.  "LLM context parallel production guide", 因果 Attention
  * 会制造 Rank 负载不均: monitor effective QK blocks per rank, not tokens.
  * Key tiles are counted as cut from each run (the bf16 tensor-core forward
- * may run fewer: it gathers the ragged tails of a query tile's unmasked runs
- * into shared key tiles).  Host only. */
+ * and dQ kernels may run fewer: they gather the ragged tails of a query
+ * tile's unmasked runs into shared key tiles).  Host only. */
 cp_status_t cp_rank_block_counts(const cp_desc_t* desc, int64_t* counts);
 
 /* Key tiles the forward (cp_attn_fwd) runs per virtual rank for one head,
- * host array of C int64: cp_rank_block_counts' tiles, less those saved by
- * gathering, when the bf16 tensor-core kernel runs the desc, the ragged
- * tails of each query tile's fully visible runs into shared key tiles
- * (pieces from 8-row boundaries, split across two tiles where one fills).
+ * host array of C int64; the dQ pass of the backward runs the same.  With
+ * the bf16 tensor-core kernels this is cp_rank_block_counts less the tiles
+ * saved by gathering the ragged tails of each query tile's fully visible
+ * runs into shared key tiles (pieces from 8-row boundaries, split across two
+ * tiles where one fills); otherwise it equals cp_rank_block_counts.
  * Host only. */
 cp_status_t cp_rank_fwd_key_tiles(const cp_desc_t* desc, int64_t* counts);
 
