@@ -76,15 +76,16 @@ enum WaitSite : int {
   kSiteDrain, kSiteAlign, kSiteStat, kSiteKVFull, kSiteKVEmpty, kSiteQ,
 };
 
-// Boxes of 8, 16, ..., 120 rows of K and V for the pieces of gathered key
-// tiles (kRangePacked runs of the dQ kernel's plan): a piece of r rows (a
-// multiple of 8) is one box per panel (map r / 8 - 1; the 128-row maps for
-// r = 128).
+// Boxes of 8, 16, ..., 120 rows for the pieces of gathered tiles
+// (kRangePacked runs): K and V for the dQ kernel's key tiles, Q and dO for
+// the dK/dV kernel's query tiles.  A piece of r rows (a multiple of 8) is one
+// box per panel (map r / 8 - 1; the 128-row maps for r = 128).
 constexpr int kPieceMaps = 15;
 
 struct BwdParams {
   CUtensorMap tq, tk, tv, tdo;
   CUtensorMap tkp[kPieceMaps], tvp[kPieceMaps];  // box rows 8 (i + 1); dQ with gathered tiles only
+  CUtensorMap tqp[kPieceMaps], top[kPieceMaps];  // the same for Q and dO; dK/dV with gathered tiles only
   AttnArgs a;
   int32_t* err;
 };
@@ -199,6 +200,8 @@ struct StepCursor {
     if (count > 0) cur = r[0];
   }
   __device__ int head() const { return inter ? g * hkv + kvh : kvh * G + g; }
+  // a gathered query tile (packed()) has its pieces from entry row0
+  __device__ bool packed() const { return (cur.flags & kRangePacked) != 0; }
   __device__ int row() const { return cur.row0 + off; }
   __device__ int n() const { return min(BNQ, cur.nrows - off); }
   __device__ int pos() const { return cur.pos0 + off; }
@@ -226,12 +229,27 @@ __device__ __forceinline__ int count_steps(const RangeDesc* ranges, int begin, i
 
 // Negated statistic of query column t (0..BNQ-1: -lse * log2e;
 // BNQ..2BNQ-1: -D * scale) of the step the cursor points at.  Stored negated
-// so that a pair of them is directly the addend of a packed FMA.
-template <int BNQ>
+// so that a pair of them is directly the addend of a packed FMA.  In a
+// gathered query tile a column that holds no query gets -lse = -inf, so that
+// its P = exp2(s * scale * log2e - inf) is exactly 0 and so is its dS.
+template <int BNQ, bool PACKED>
 __device__ __forceinline__ float load_stat(const AttnArgs& a, const StepCursor<BNQ>& c, int t) {
   const int col = t % BNQ;
-  if (t >= 2 * BNQ || col >= c.n()) return 0.f;
-  const int64_t idx = int64_t(c.head()) * a.T + c.row() + col;
+  if (t >= 2 * BNQ) return 0.f;
+  int64_t row;
+  if (PACKED && c.packed()) {
+    row = -1;
+    const int count = c.cur.flags >> kPackCountShift;
+    for (int i = 0; i < count; ++i) {
+      const PackPiece pc = a.pieces[c.cur.row0 + i];
+      if (col >= pc.dst && col < pc.dst + pc.keys) row = int64_t(pc.src) + (col - pc.dst);
+    }
+    if (row < 0) return t < BNQ ? -INFINITY : 0.f;
+  } else {
+    if (col >= c.n()) return 0.f;
+    row = c.row() + col;
+  }
+  const int64_t idx = int64_t(c.head()) * a.T + row;
   return t < BNQ ? -(a.lse_in[idx] * kLog2e) : -(a.dpsum[idx] * a.scale);
 }
 
@@ -289,7 +307,9 @@ struct DkdvCfg {
   static_assert(kSmem <= 232448, "shared memory budget");
 };
 
-template <int DQK, int BNQ>
+// PACKED: the plan has gathered query tiles (kRangePacked runs, 128-row steps
+// only); plans without them run an instantiation without that code.
+template <int DQK, int BNQ, bool PACKED>
 __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dkdv_kernel(const __grid_constant__ BwdParams p) {
   using Cfg = DkdvCfg<DQK, BNQ>;
   constexpr int NC = Cfg::kCols;
@@ -358,6 +378,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dkdv_kernel(const __grid
     ptx::prefetch_tmap(&p.tv);
     ptx::prefetch_tmap(&p.tdo);
   }
+  if (PACKED && warp == 8 && lane >= 2)  // the piece maps, one per lane
+    ptx::prefetch_tmap(lane < 2 + kPieceMaps ? &p.tqp[lane - 2] : &p.top[lane - 2 - kPieceMaps]);
   ptx::tc_fence_before();
   __syncthreads();
   ptx::tc_fence_after();
@@ -388,16 +410,24 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dkdv_kernel(const __grid
         // stage st is free once the last reader of its previous occupant completed
         if (i >= NS && !ptx::mbar_wait(empty(st), ((i / NS) - 1) & 1, kSiteQEmpty, wctx)) break;
         const int h = cur.head();
-        if (qstream) {
-          ptx::mbar_arrive_expect_tx(full(st), Cfg::kQBytes);
-          for (int c = 0; c < Cfg::kKPanels; ++c)
-            ptx::tma_load_3d(sbase + Cfg::offQ + st * Cfg::kQBytes + c * Cfg::kQPanel, &p.tq, full(st), c * 64, h,
-                             cur.row());
+        const uint32_t dst0 = sbase + (qstream ? Cfg::offQ + st * Cfg::kQBytes : Cfg::offO + st * Cfg::kOBytes);
+        const int panels = qstream ? Cfg::kKPanels : 2;
+        const CUtensorMap* map = qstream ? &p.tq : &p.tdo;
+        ptx::mbar_arrive_expect_tx(full(st), qstream ? Cfg::kQBytes : Cfg::kOBytes);
+        if (!PACKED || !cur.packed()) {
+          for (int c = 0; c < panels; ++c)
+            ptx::tma_load_3d(dst0 + c * Cfg::kQPanel, map, full(st), c * 64, h, cur.row());
         } else {
-          ptx::mbar_arrive_expect_tx(full(st), Cfg::kOBytes);
-          for (int c = 0; c < 2; ++c)
-            ptx::tma_load_3d(sbase + Cfg::offO + st * Cfg::kOBytes + c * Cfg::kQPanel, &p.tdo, full(st), c * 64, h,
-                             cur.row());
+          // one box per piece; the pieces cover rows [0, BNQ) of the step
+          // from 8-row (1 KiB) boundaries
+          const CUtensorMap* maps = qstream ? p.tqp : p.top;
+          const int count = cur.cur.flags >> kPackCountShift;
+          for (int k = 0; k < count; ++k) {
+            const PackPiece pc = a.pieces[cur.cur.row0 + k];
+            const CUtensorMap* m = pc.rows >= BNQ ? map : maps + (max(pc.rows, 8) >> 3) - 1;
+            for (int c = 0; c < panels; ++c)
+              ptx::tma_load_3d(dst0 + c * Cfg::kQPanel + uint32_t(pc.dst) * 128, m, full(st), c * 64, h, pc.src);
+          }
         }
         ++issued;
       }
@@ -502,7 +532,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dkdv_kernel(const __grid
     cur.init(a.ranges, tile.range_begin, tile.range_count, G, kvh, a.hkv, a.gqa_interleaved);
     nxt = cur;
     if (n_steps > 0) {
-      if (t < 2 * BNQ) stat[t] = load_stat<BNQ>(a, cur, t);
+      if (t < 2 * BNQ) stat[t] = load_stat<BNQ, PACKED>(a, cur, t);
       ptx::mbar_arrive(bar_stat(0));
     }
     nxt.next();
@@ -516,9 +546,12 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dkdv_kernel(const __grid
         ok = false;
         break;
       }
-      const float nstat = (i + 1 < n_steps) ? load_stat<BNQ>(a, nxt, t) : 0.f;
-      const bool need_mask = nq < BNQ || nk < BT || (a.causal && qpos0 < tile.pos0 + BT - 1);
-      const int cmin = (a.causal ? kpos - qpos0 : 0) - int(colS);  // first visible column (relative)
+      const float nstat = (i + 1 < n_steps) ? load_stat<BNQ, PACKED>(a, nxt, t) : 0.f;
+      // a gathered query tile is causally unmasked; its query-less columns
+      // have P = 0 through their statistics
+      const bool causal = a.causal && !(PACKED && cur.packed());
+      const bool need_mask = nq < BNQ || nk < BT || (causal && qpos0 < tile.pos0 + BT - 1);
+      const int cmin = (causal ? kpos - qpos0 : 0) - int(colS);  // first visible column (relative)
       const int cmax = (r < nk ? nq : 0) - int(colS);             // columns [cmin, cmax) are visible
 
       // ---- P^T = exp(S^T * scale - lse)
@@ -1049,12 +1082,21 @@ cudaError_t launch_dkdv(const AttnArgs& a, cudaStream_t st) {
   p.a = a;
   p.err = device_error_word();
   if (!make_maps(p, a, DQK, BNQ)) return cudaErrorInvalidValue;
-  cudaError_t e = cudaFuncSetAttribute(attn_bwd_dkdv_kernel<DQK, BNQ>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       int(Cfg::kSmem));
+  if (a.num_packs > 0) {
+    if (BNQ != 128) return cudaErrorInvalidValue;  // gathered query tiles are 128 rows
+    for (int m = 0; m < kPieceMaps; ++m)
+      if (!make_map_3d(&p.tqp[m], a.q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, DQK, a.hq, a.T, 64, 8 * (m + 1),
+                       CU_TENSOR_MAP_SWIZZLE_128B) ||
+          !make_map_3d(&p.top[m], a.dout, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, DV, a.hq, a.T, 64, 8 * (m + 1),
+                       CU_TENSOR_MAP_SWIZZLE_128B))
+        return cudaErrorInvalidValue;
+  }
+  auto kernel = a.num_packs > 0 ? attn_bwd_dkdv_kernel<DQK, BNQ, true> : attn_bwd_dkdv_kernel<DQK, BNQ, false>;
+  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(Cfg::kSmem));
   if (e != cudaSuccess) return e;
   const int64_t grid = int64_t(a.num_tiles) * a.hkv;
   if (grid == 0) return cudaSuccess;
-  attn_bwd_dkdv_kernel<DQK, BNQ><<<unsigned(grid), kThreads, Cfg::kSmem, st>>>(p);
+  kernel<<<unsigned(grid), kThreads, Cfg::kSmem, st>>>(p);
   return cudaGetLastError();
 }
 

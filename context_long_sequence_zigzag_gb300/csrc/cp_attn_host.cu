@@ -328,7 +328,7 @@ Plan build_fwd_plan(const cp_desc_t* d, const ShardMap& m, int q_rank, int kv_ra
 
 // Key-major plan for the backward: every key tile with the query runs that
 // see it, visiting ranks r, r+1, ... (the direction dK/dV travel in a ring).
-Plan build_bwd_plan(const cp_desc_t* d, const ShardMap& m) {
+Plan build_bwd_plan(const cp_desc_t* d, const ShardMap& m, bool pack = false) {
   Plan p;
   const bool causal = d->causal != 0;
   for (const Chunk& B : m.chunks) {
@@ -377,6 +377,11 @@ Plan build_bwd_plan(const cp_desc_t* d, const ShardMap& m) {
         }
         for (size_t i = first; i < p.ranges.size(); ++i) work += ceil_tiles(p.ranges[i].nrows);
       }
+      if (pack) {  // the tails of the query runs that see the whole key tile
+        pack_tails(p, size_t(t.range_begin));
+        work = 0;
+        for (size_t i = size_t(t.range_begin); i < p.ranges.size(); ++i) work += ceil_tiles(p.ranges[i].nrows);
+      }
       t.range_count = int32_t(p.ranges.size()) - t.range_begin;
       t.work = work;
       p.max_ranges = std::max(p.max_ranges, t.range_count);
@@ -407,8 +412,11 @@ size_t plan_bytes(const Plan& p) {
 // happens every call, since the caller may use that memory for anything in
 // between.
 // kPlanQueryMajorPacked: the query-major plan with the unmasked runs' tails
-// gathered into shared key tiles (the tensor-core forward reads those).
-enum PlanKind : int64_t { kPlanQueryMajor = 0, kPlanKeyMajor = 1, kPlanQueryMajorPacked = 2 };
+// gathered into shared key tiles (the tensor-core forward and dQ kernels
+// read those); kPlanKeyMajorPacked: the key-major plan with the tails of
+// the query runs that see a whole key tile gathered into shared query tiles
+// (the tensor-core dK/dV kernel with 128-row query steps).
+enum PlanKind : int64_t { kPlanQueryMajor = 0, kPlanKeyMajor = 1, kPlanQueryMajorPacked = 2, kPlanKeyMajorPacked = 3 };
 std::shared_ptr<const Plan> get_plan(const cp_desc_t* d, const ShardMap& m, PlanKind kind, int q_rank = -1,
                                      int kv_rank = -1, int ring_step = -1, int64_t slot_rows = 0) {
   static std::mutex mu;
@@ -427,10 +435,10 @@ std::shared_ptr<const Plan> get_plan(const cp_desc_t* d, const ShardMap& m, Plan
         return it->second;
       }
   }
-  auto plan = std::make_shared<Plan>(kind == kPlanKeyMajor
-                                         ? build_bwd_plan(d, m)
-                                         : build_fwd_plan(d, m, q_rank, kv_rank, ring_step, slot_rows,
-                                                          kind == kPlanQueryMajorPacked));
+  const bool key_major = kind == kPlanKeyMajor || kind == kPlanKeyMajorPacked;
+  auto plan = std::make_shared<Plan>(key_major ? build_bwd_plan(d, m, kind == kPlanKeyMajorPacked)
+                                               : build_fwd_plan(d, m, q_rank, kv_rank, ring_step, slot_rows,
+                                                                kind == kPlanQueryMajorPacked));
   order_by_work(*plan);
   std::lock_guard<std::mutex> lock(mu);
   cache.emplace_front(std::move(key), plan);
@@ -617,6 +625,10 @@ bool use_tc_bwd(const cp_desc_t* d) {
 // gathered key tiles.
 PlanKind fwd_plan_kind(const cp_desc_t* d) { return use_tc_fwd(d) ? kPlanQueryMajorPacked : kPlanQueryMajor; }
 PlanKind dq_plan_kind(const cp_desc_t* d) { return use_tc_bwd(d) ? kPlanQueryMajorPacked : kPlanQueryMajor; }
+// The dK/dV kernel's: gathered query tiles where its query steps are 128 rows.
+PlanKind dkdv_plan_kind(const cp_desc_t* d) {
+  return use_tc_bwd(d) && d->d_qk == 128 ? kPlanKeyMajorPacked : kPlanKeyMajor;
+}
 
 AttnArgs base_args(const cp_desc_t* d) {
   AttnArgs a{};
@@ -636,7 +648,7 @@ AttnArgs base_args(const cp_desc_t* d) {
 // Uploads the key-major plan into `ws` and launches the dK/dV kernel.
 cp_status_t run_bwd_dkdv(const cp_desc_t* d, const ShardMap& m, AttnArgs a, char* ws, size_t ws_bytes,
                          cudaStream_t cs) {
-  const auto pbp = get_plan(d, m, kPlanKeyMajor);
+  const auto pbp = get_plan(d, m, dkdv_plan_kind(d));
   const Plan& pb = *pbp;
   if (ws == nullptr || (reinterpret_cast<uintptr_t>(ws) & 255) || ws_bytes < plan_bytes(pb)) return CP_ERR_WORKSPACE;
   const cp_status_t st = stage_plan(pb, ws, cs, a, d->total_tokens, d->total_tokens);
@@ -963,9 +975,9 @@ cp_status_t cp_workspace_size(const cp_desc_t* d, int32_t op, size_t* bytes) {
     for (int r = 0; r < m.C; ++r) mx = std::max(mx, plan_bytes(build_fwd_plan(d, m, r, -1)));
     *bytes = mx;
   } else if (op == CP_OP_BWD) {
-    *bytes = bwd_layout(d, *get_plan(d, m, dq_plan_kind(d)), *get_plan(d, m, kPlanKeyMajor)).total;
+    *bytes = bwd_layout(d, *get_plan(d, m, dq_plan_kind(d)), *get_plan(d, m, dkdv_plan_kind(d))).total;
   } else if (op == CP_OP_BWD_DKDV) {
-    *bytes = plan_bytes(*get_plan(d, m, kPlanKeyMajor));
+    *bytes = plan_bytes(*get_plan(d, m, dkdv_plan_kind(d)));
   } else if (op == CP_OP_BWD_DQ) {
     *bytes = plan_bytes(*get_plan(d, m, dq_plan_kind(d)));
   } else if (op == CP_OP_RING_FWD) {
@@ -1148,7 +1160,7 @@ cp_status_t cp_attn_bwd(const cp_desc_t* d, const void* q, const void* k, const 
     if (p == nullptr || !aligned16(p)) return CP_ERR_INVALID_ARG;
   ShardMap m = build_map(d);
   const auto pfp = get_plan(d, m, dq_plan_kind(d));
-  const auto pbp = get_plan(d, m, kPlanKeyMajor);
+  const auto pbp = get_plan(d, m, dkdv_plan_kind(d));
   const Plan& pf = *pfp;
   const Plan& pb = *pbp;
   BwdLayout L = bwd_layout(d, pf, pb);
