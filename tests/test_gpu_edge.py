@@ -6,7 +6,8 @@ tiling: empty sequences in cu_seqlens, sequences shorter than 2C (empty
 zigzag chunks on some virtual ranks), one token, 64 virtual ranks with
 chunks far below a 128-row tile, GQA ratios 3:1 and 8:1, sequence isolation
 without the causal mask, bf16 heads the tensor-core kernels do not take (the
-CUDA-core path), and a softmax scale other than 1/sqrt(d).  Tolerances as
+CUDA-core path), a softmax scale other than 1/sqrt(d), and plans whose key
+and query tiles are gathered from many run tails.  Tolerances as
 everywhere: bf16 o max-abs 2e-2, lse 1e-3, gradients relative Frobenius
 2e-2; fp32 max-abs 1e-5.
 """
@@ -48,7 +49,15 @@ CASES = {
                           seqlens=(1000, 300), sigma=0.5),
     "f32_c16": dict(total_tokens=333, hq=2, hkv=1, d_qk=64, d_v=64, cp_size=16, layout="zigzag", dtype="f32",
                     seqlens=(200, 0, 133)),
+    # gathered tiles: many run tails per tile (pieces from 1 to 127 rows, some
+    # split across two tiles, some filled from rows past the tensor's end)
+    "gathered_short_seqs": dict(total_tokens=4183, hq=4, hkv=2, d_qk=128, d_v=128, cp_size=4, layout="zigzag",
+                                seqlens=(9, 17, 33, 65, 130, 260, 520, 1040, 2109)),
+    "gathered_contiguous": dict(total_tokens=2501, hq=2, hkv=1, d_qk=128, d_v=128, cp_size=8, layout="contiguous",
+                                seqlens=(1500, 700, 301)),
 }
+
+GATHERED = ("gathered_short_seqs", "gathered_contiguous", "noncausal_varlen")
 
 
 def _setup(kw, scale=None):
@@ -86,6 +95,8 @@ def _check(w, inp, cu, perm, sc, f32, o, lse, grads=None):
 @pytest.mark.parametrize("name", list(CASES))
 def test_forward_backward_edge(name):
     w, inp, cu, perm, prob, sh, sc, f32 = _setup(CASES[name])
+    if name in GATHERED:  # the tensor-core kernels run gathered tiles here
+        assert sum(cpa.cp_rank_fwd_key_tiles(prob)) < sum(cpa.cp_rank_block_counts(prob))
     o, lse = cpa.cp_attn_fwd(prob, sh["q"], sh["k"], sh["v"])
     grads = cpa.cp_attn_bwd(prob, sh["q"], sh["k"], sh["v"], o, lse, sh["dout"])
     torch.cuda.synchronize()
