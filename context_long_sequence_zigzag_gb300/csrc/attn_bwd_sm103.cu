@@ -48,6 +48,13 @@
 // elect one lane per instruction.  The P and dS loops use packed f32x2
 // arithmetic; dK/dV stages its per-column statistics negated so that a float4
 // of them is two packed addends.
+//
+// Gathered tiles (plan runs of kind kRangePacked; a separate instantiation of
+// each kernel): the dQ kernel's key tiles and the dK/dV kernel's query tiles
+// may hold the ragged tails of several fully visible runs, one TMA box per
+// piece.  dQ masks their key-less columns from a per-tile key mask; dK/dV
+// gives a query-less column the statistic -lse = -inf, so that its P and dS
+// are exactly zero.
 #include <cuda.h>
 #include <cuda_bf16.h>
 

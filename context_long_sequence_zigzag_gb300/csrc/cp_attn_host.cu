@@ -187,6 +187,7 @@ struct Plan {
   std::vector<RangeDesc> ranges;
   std::vector<PackMask> packs;  // key masks of the gathered key tiles (kRangePacked runs)
   std::vector<PackPiece> pieces;
+  std::vector<int32_t> tile_seq;  // key-major plans: each tile's sequence (host only, for the order)
   int32_t max_ranges = 0;
 };
 
@@ -386,16 +387,45 @@ Plan build_bwd_plan(const cp_desc_t* d, const ShardMap& m, bool pack = false) {
       t.work = work;
       p.max_ranges = std::max(p.max_ranges, t.range_count);
       p.tiles.push_back(t);
+      p.tile_seq.push_back(B.seq);
     }
   }
   return p;
 }
 
 // Heaviest tiles first, so that the block scheduler starts the long ones
-// early (longest-processing-time order).
+// early (longest-processing-time order).  A key-major plan of several
+// sequences goes sequence by sequence instead (heaviest sequence first,
+// heaviest tiles first inside each): its CTAs read the Q and dO of their
+// own sequence, so the resident CTAs then share the Q and dO of a few
+// sequences in L2 instead of touching every sequence's (in work order the
+// dK/dV kernel read 5.7x its algorithmic bytes on a 128K-token pack of 16
+// sequences).  With one sequence both orders are the same.
 void order_by_work(Plan& p) {
-  std::stable_sort(p.tiles.begin(), p.tiles.end(),
-                   [](const TileDesc& a, const TileDesc& b) { return a.work > b.work; });
+  if (p.tile_seq.size() != p.tiles.size() || p.tiles.empty()) {
+    std::stable_sort(p.tiles.begin(), p.tiles.end(),
+                     [](const TileDesc& a, const TileDesc& b) { return a.work > b.work; });
+    return;
+  }
+  const int32_t nseq = *std::max_element(p.tile_seq.begin(), p.tile_seq.end()) + 1;
+  std::vector<int64_t> seq_work(size_t(nseq), 0);
+  for (size_t i = 0; i < p.tiles.size(); ++i) seq_work[size_t(p.tile_seq[i])] += p.tiles[i].work;
+  std::vector<size_t> idx(p.tiles.size());
+  for (size_t i = 0; i < idx.size(); ++i) idx[i] = i;
+  std::stable_sort(idx.begin(), idx.end(), [&](size_t a, size_t b) {
+    const int32_t sa = p.tile_seq[a], sb = p.tile_seq[b];
+    if (sa != sb) return seq_work[size_t(sa)] != seq_work[size_t(sb)] ? seq_work[size_t(sa)] > seq_work[size_t(sb)]
+                                                                      : sa < sb;
+    return p.tiles[a].work > p.tiles[b].work;
+  });
+  std::vector<TileDesc> tiles(p.tiles.size());
+  std::vector<int32_t> seqs(p.tiles.size());
+  for (size_t i = 0; i < idx.size(); ++i) {
+    tiles[i] = p.tiles[idx[i]];
+    seqs[i] = p.tile_seq[idx[i]];
+  }
+  p.tiles.swap(tiles);
+  p.tile_seq.swap(seqs);
 }
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
