@@ -193,17 +193,18 @@ struct Plan {
 
 int32_t round8(int32_t n) { return (n + 7) & ~7; }
 
-// Gathers the ragged tails of a query tile's unmasked runs into shared key
-// tiles.  Every key of an unmasked run is visible to every row of the tile,
-// so where a key sits in the tile does not matter: each run keeps its whole
+// Gathers the ragged tails of one tile's unmasked runs (key runs of a query
+// tile, or query runs of a key tile) into shared tiles.  In an unmasked run
+// every pair with the tile's rows is visible, so where a run's row sits in
+// the tile it is cut into does not matter: each run keeps its whole
 // kTile-row steps as a run of its own, and the tails (fewer than kTile rows
 // each) are laid back to back from 8-row boundaries, split across two tiles
-// where one fills up.  The rows between a tail's last key and the next
-// boundary, and after the last tail up to the tile's end, are loaded from
-// the rows that follow it and masked.  Done only where it saves key tiles:
-// where the tails would need as many tiles gathered as apart, nothing changes.  Returns the tile's runs
-// (masked runs first, as built, then the whole steps, then the gathered
-// tiles) in place of [first, end) of p.ranges.
+// where one fills up.  The rows between a tail's last row and the next
+// boundary, and after the last tail up to the tile's end, are loaded from the
+// rows that follow it and masked.  Done only where it saves tiles: where the
+// tails would need as many tiles gathered as apart, nothing changes.  The
+// tile's runs [first, end) of p.ranges become its masked and whole-step runs,
+// in their order, followed by the gathered tiles.
 void pack_tails(Plan& p, size_t first) {
   std::vector<RangeDesc> keep;
   std::vector<std::pair<int32_t, int32_t>> tails;  // (first sharded row, rows)
