@@ -152,10 +152,12 @@ def chosen_workload(args) -> workloads.Workload:
         if hq < 1 or hkv < 1 or hq % hkv:
             raise SystemExit("--heads wants HQ:HKV with HKV dividing HQ")
         kw["hq"], kw["hkv"] = hq, hkv
-    if args.seq_len:
-        if w.seqlens is not None or w.varlen_range is not None:
-            raise SystemExit("--seq-len applies to single-sequence workloads")
-        kw["total_tokens"] = args.seq_len
+    if args.seq_len is not None:
+        if args.seq_len < 1:
+            raise SystemExit("--seq-len wants a positive token count")
+        if w.seqlens is not None:
+            raise SystemExit("--seq-len does not apply to a workload with fixed sequence lengths")
+        kw["total_tokens"] = args.seq_len  # a varlen pack is drawn to this many tokens
     if not kw:
         return w
     tag = ",".join(f"{k}={v}" for k, v in kw.items())
@@ -851,7 +853,8 @@ def main():
                     help="skip the throughput lines of the other standard problems")
     ap.add_argument("--layout", default=None, choices=["contiguous", "zigzag", "striped"],
                     help="shard layout instead of the workload's own (zigzag for the standard ones)")
-    ap.add_argument("--seq-len", type=int, default=None, help="sequence length (single-sequence workloads)")
+    ap.add_argument("--seq-len", type=int, default=None,
+                    help="sequence length (single-sequence workloads) or total tokens of a varlen pack")
     ap.add_argument("--heads", default=None, help="query:key-value head counts, e.g. 32:8")
     ap.add_argument("--cp-size", type=int, default=None, help="number of context-parallel shards C")
     ap.add_argument("--seed", type=int, default=None, help="input generator seed")

@@ -54,6 +54,14 @@ def test_reference_arm_takes_the_overrides():
 def test_bad_override_is_refused():
     p = _run(["--impl", "reference", "--steps", "1", "--warmup", "0", "--heads", "6:4"])
     assert p.returncode != 0
-    p = _run(["--impl", "reference", "--steps", "1", "--warmup", "0", "--workload",
-              "bf16_varlen_t128k_h16kv4_d128_c16_zigzag", "--seq-len", "1024"])
+    p = _run(["--impl", "reference", "--steps", "1", "--warmup", "0", "--seq-len", "-5"])
     assert p.returncode != 0
+
+
+def test_varlen_pack_takes_a_token_count():
+    p = _run(["--impl", "reference", "--steps", "1", "--warmup", "0", "--cpu-tokens", "256", "--workload",
+              "bf16_varlen_t128k_h16kv4_d128_c16_zigzag", "--seq-len", "32768"])
+    assert p.returncode == 0, p.stderr[-2000:]
+    d = json.loads([l for l in p.stdout.splitlines() if l.startswith("{")][0])
+    assert d["config"]["total_tokens"] == 32768
+    assert d["config"]["workload"] == "bf16_varlen_t128k_h16kv4_d128_c16_zigzag[total_tokens=32768]"
